@@ -1,0 +1,328 @@
+/*
+ * tree_attn_oracle.c -- fp64 CPU oracle for split tree attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * What it computes (source: "Efficient Speculative Decoding for Llama at
+ * Scale", pith.science review page 2508.08192, section "What carries the
+ * argument"): the draft tree is flattened into one sequence of T tokens; each
+ * tree token attends to the whole committed prefix with no mask and to the
+ * tree tokens allowed by the tree mask.  Split tree attention computes the
+ * prefix piece and the tree piece separately and merges them
+ * ("merge_attentions", pith.science verdict record, supporting_citations:
+ * the way to combine attention over disjoint KV chunks).  Because the merge is
+ * exact, the plain definition is ONE softmax over the union of both key sets,
+ * which is what oracle_verify_rows writes out, in double precision, with no
+ * splitting.
+ *
+ * Readings where the pages are silent (each one is also listed in the design
+ * notes):
+ *   - scores are softmax_scale * <q, k>; the scale is an argument;
+ *   - query head h reads KV head h / G, G = Hq / Hkv (contiguous groups);
+ *   - bit j of mask[i] set  <=>  tree token i may attend to tree token j;
+ *     bits at positions >= T are ignored;
+ *   - lse is the natural log of the softmax denominator over all attended
+ *     keys;
+ *   - prefix token p of sequence b lives in physical page
+ *     block_table[b][p / P], slot p % P, with pages laid out
+ *     [num_pages][Hkv][P][d];
+ *   - a row with no attended key returns out = 0, lse = -inf.
+ *
+ * Inputs are raw bf16 bit patterns (uint16); each value is widened exactly to
+ * double before any arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Error codes returned by the oracle entry points. */
+#define ORACLE_OK 0
+#define ORACLE_BAD_PARENT (-1)
+#define ORACLE_BAD_PAGE (-2)
+#define ORACLE_BAD_ARG (-3)
+#define ORACLE_NO_MEMORY (-4)
+
+/* Exact bf16 -> double: a bf16 value is the upper half of an IEEE binary32. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Tree mask from a parent array (tree mask: pith.science review, "What
+ * carries the argument"; flattened-draft verification after SpecInfer, Miao
+ * et al., cited in the verdict record's supporting_citations).
+ *
+ * Node i may see itself and every ancestor.  The oracle walks the parent
+ * pointers from i up to the root and sets one bit per node on the way.
+ * parents[i] must be -1 (a root) or an earlier node; anything else is an
+ * error.  T may be 1..64.
+ */
+int oracle_tree_mask(const int32_t *parents, int T, uint64_t *mask) {
+    if (T < 1 || T > 64) return ORACLE_BAD_ARG;
+    for (int i = 0; i < T; ++i) {
+        if (parents[i] < -1 || parents[i] >= i) return ORACLE_BAD_PARENT;
+    }
+    for (int i = 0; i < T; ++i) {
+        uint64_t bits = 0;
+        int node = i;
+        while (node != -1) {
+            bits |= (uint64_t)1 << node;
+            node = parents[node];
+        }
+        mask[i] = bits;
+    }
+    return ORACLE_OK;
+}
+
+/* Shapes and pointers of one verification call. */
+typedef struct {
+    const uint16_t *q;           /* [B][T][Hq][d]              */
+    const uint16_t *k_pages;     /* [num_pages][Hkv][P][d]     */
+    const uint16_t *v_pages;     /* [num_pages][Hkv][P][d]     */
+    const int32_t *block_table;  /* [B][max_pages_per_seq]     */
+    const int32_t *seq_lens;     /* [B]                        */
+    const uint16_t *tree_k;      /* [B][T][Hkv][d]             */
+    const uint16_t *tree_v;      /* [B][T][Hkv][d]             */
+    const uint64_t *mask;        /* [T]                        */
+    int B, Hq, Hkv, d, T, P, num_pages, max_pages_per_seq;
+    double scale;
+} oracle_call;
+
+/*
+ * Attention of query row (b, i, h) over one chunk of its keys: the prefix
+ * tokens p in [p_begin, p_end) (clipped to the sequence length) and, when
+ * use_tree is set, the tree tokens that mask[i] allows.
+ *
+ *   s_k   = scale * <q_{b,i,h}, key_k>
+ *   mu    = max_k s_k
+ *   lse   = mu + ln sum_k exp(s_k - mu)
+ *   out   = sum_k exp(s_k - lse) * value_k
+ *
+ * An empty chunk gives out = 0, lse = -inf.  `scores` must hold at least
+ * (p_end - p_begin) + T doubles.
+ */
+static int attend_chunk(const oracle_call *c, int b, int i, int h,
+                        long p_begin, long p_end, int use_tree,
+                        double *scores, double *qrow, double *out, double *lse) {
+    const int d = c->d;
+    const int G = c->Hq / c->Hkv;
+    const int hk = h / G;
+    long L = c->seq_lens[b];
+    if (L < 0) return ORACLE_BAD_ARG;
+    if (p_end > L) p_end = L;
+    if (p_begin < 0) p_begin = 0;
+    const uint64_t row_mask = c->mask[i];
+
+    const uint16_t *qp = c->q + (((size_t)b * c->T + i) * c->Hq + h) * d;
+    for (int x = 0; x < d; ++x) qrow[x] = bf16_to_double(qp[x]);
+
+    /* Pass 1: the scores, prefix keys first, then tree keys. */
+    long n = 0;
+    for (long p = p_begin; p < p_end; ++p) {
+        long slot = p / c->P;
+        if (slot >= c->max_pages_per_seq) return ORACLE_BAD_ARG;
+        int32_t page = c->block_table[(size_t)b * c->max_pages_per_seq + slot];
+        if (page < 0 || page >= c->num_pages) return ORACLE_BAD_PAGE;
+        const uint16_t *kp = c->k_pages + (((size_t)page * c->Hkv + hk) * c->P + (p % c->P)) * d;
+        double dot = 0.0;
+        for (int x = 0; x < d; ++x) dot += qrow[x] * bf16_to_double(kp[x]);
+        scores[n++] = c->scale * dot;
+    }
+    if (use_tree) {
+        for (int j = 0; j < c->T; ++j) {
+            if (((row_mask >> j) & 1u) == 0) continue;
+            const uint16_t *kp = c->tree_k + (((size_t)b * c->T + j) * c->Hkv + hk) * d;
+            double dot = 0.0;
+            for (int x = 0; x < d; ++x) dot += qrow[x] * bf16_to_double(kp[x]);
+            scores[n++] = c->scale * dot;
+        }
+    }
+
+    for (int x = 0; x < d; ++x) out[x] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return ORACLE_OK;
+    }
+
+    /* Pass 2: log-sum-exp of the scores. */
+    double mu = scores[0];
+    for (long k = 1; k < n; ++k) if (scores[k] > mu) mu = scores[k];
+    double Z = 0.0;
+    for (long k = 0; k < n; ++k) Z += exp(scores[k] - mu);
+    const double row_lse = mu + log(Z);
+    *lse = row_lse;
+
+    /* Pass 3: probability-weighted sum of the values, same key order. */
+    long k = 0;
+    for (long p = p_begin; p < p_end; ++p, ++k) {
+        int32_t page = c->block_table[(size_t)b * c->max_pages_per_seq + p / c->P];
+        const uint16_t *vp = c->v_pages + (((size_t)page * c->Hkv + hk) * c->P + (p % c->P)) * d;
+        const double w = exp(scores[k] - row_lse);
+        for (int x = 0; x < d; ++x) out[x] += w * bf16_to_double(vp[x]);
+    }
+    if (use_tree) {
+        for (int j = 0; j < c->T; ++j) {
+            if (((row_mask >> j) & 1u) == 0) continue;
+            const uint16_t *vp = c->tree_v + (((size_t)b * c->T + j) * c->Hkv + hk) * d;
+            const double w = exp(scores[k] - row_lse);
+            for (int x = 0; x < d; ++x) out[x] += w * bf16_to_double(vp[x]);
+            ++k;
+        }
+    }
+    return ORACLE_OK;
+}
+
+static int check_call(const oracle_call *c) {
+    if (c->B < 0 || c->T < 1 || c->T > 64 || c->Hkv < 1 || c->Hq < c->Hkv ||
+        c->Hq % c->Hkv != 0 || c->d < 1 || c->P < 1 || c->num_pages < 0)
+        return ORACLE_BAD_ARG;
+    return ORACLE_OK;
+}
+
+/*
+ * Split-free tree attention for a list of query rows.
+ *
+ * rows[3*r .. 3*r+2] = (b, i, h).  For each row the key set is every prefix
+ * token of sequence b plus the tree tokens allowed by mask[i]; out[r][0..d)
+ * and lse[r] receive the softmax-weighted value sum and the natural-log
+ * normaliser.  Rows are independent; they are spread over `threads` OpenMP
+ * threads (<= 0: the OpenMP default).  Returns 0 or the first error code.
+ */
+int oracle_verify_rows(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                       const int32_t *block_table, int max_pages_per_seq,
+                       const int32_t *seq_lens, const uint16_t *tree_k, const uint16_t *tree_v,
+                       const uint64_t *mask, int B, int Hq, int Hkv, int d, int T, int P,
+                       int num_pages, double scale, const int32_t *rows, long n_rows,
+                       double *out, double *lse, int threads) {
+    oracle_call c = {q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, mask,
+                     B, Hq, Hkv, d, T, P, num_pages, max_pages_per_seq, scale};
+    if (check_call(&c) != ORACLE_OK) return ORACLE_BAD_ARG;
+    long max_L = 0;
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0) return ORACLE_BAD_ARG;
+        if (seq_lens[b] > max_L) max_L = seq_lens[b];
+    }
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#else
+    threads = 1;
+#endif
+#pragma omp parallel num_threads(threads)
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(max_L + T + 1));
+        double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
+        if (scores == NULL || qrow == NULL) {
+#pragma omp critical
+            err = ORACLE_NO_MEMORY;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long r = 0; r < n_rows; ++r) {
+                const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
+                int e = ORACLE_BAD_ARG;
+                if (b >= 0 && b < B && i >= 0 && i < T && h >= 0 && h < Hq)
+                    e = attend_chunk(&c, b, i, h, 0, seq_lens[b], 1, scores, qrow,
+                                     out + (size_t)r * d, lse + r);
+                if (e != ORACLE_OK) {
+#pragma omp critical
+                    if (err == ORACLE_OK) err = e;
+                }
+            }
+        }
+        free(scores);
+        free(qrow);
+    }
+    return err;
+}
+
+/*
+ * Attention of the same rows over ONE chunk of the keys: prefix tokens
+ * [p_begin, p_end) and, if use_tree, the tree tokens.  Used only to check the
+ * merge identity; single threaded.
+ */
+int oracle_chunk_rows(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                      const int32_t *block_table, int max_pages_per_seq,
+                      const int32_t *seq_lens, const uint16_t *tree_k, const uint16_t *tree_v,
+                      const uint64_t *mask, int B, int Hq, int Hkv, int d, int T, int P,
+                      int num_pages, double scale, const int32_t *rows, long n_rows,
+                      long p_begin, long p_end, int use_tree, double *out, double *lse) {
+    oracle_call c = {q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, mask,
+                     B, Hq, Hkv, d, T, P, num_pages, max_pages_per_seq, scale};
+    if (check_call(&c) != ORACLE_OK) return ORACLE_BAD_ARG;
+    long span = p_end > p_begin ? p_end - p_begin : 0;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(span + T + 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
+    int err = (scores && qrow) ? ORACLE_OK : ORACLE_NO_MEMORY;
+    for (long r = 0; r < n_rows && err == ORACLE_OK; ++r) {
+        const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
+        if (b < 0 || b >= B || i < 0 || i >= T || h < 0 || h >= Hq) { err = ORACLE_BAD_ARG; break; }
+        err = attend_chunk(&c, b, i, h, p_begin, p_end, use_tree, scores, qrow,
+                           out + (size_t)r * d, lse + r);
+    }
+    free(scores);
+    free(qrow);
+    return err;
+}
+
+/*
+ * merge_attentions over disjoint key chunks (pith.science verdict record,
+ * supporting_citations: Hydragen, Juravsky et al.; the same identity as the
+ * chunked softmax of Rabe & Staats).  Given per-chunk normalised outputs
+ * out_c and log-sum-exps lse_c of one query row:
+ *
+ *   lse = ln sum_c exp(lse_c)
+ *   out = sum_c exp(lse_c - lse) * out_c
+ *
+ * Chunks with lse_c = -inf hold no keys and add nothing.  outs is
+ * [n_chunks][n_rows][d], lses [n_chunks][n_rows].
+ */
+void oracle_merge(int n_chunks, long n_rows, int d, const double *outs, const double *lses,
+                  double *out, double *lse) {
+    for (long r = 0; r < n_rows; ++r) {
+        double top = -INFINITY;
+        for (int ch = 0; ch < n_chunks; ++ch) {
+            const double v = lses[(size_t)ch * n_rows + r];
+            if (v > top) top = v;
+        }
+        for (int x = 0; x < d; ++x) out[(size_t)r * d + x] = 0.0;
+        if (top == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double Z = 0.0;
+        for (int ch = 0; ch < n_chunks; ++ch) {
+            const double v = lses[(size_t)ch * n_rows + r];
+            if (v == -INFINITY) continue;
+            Z += exp(v - top);
+        }
+        const double total = top + log(Z);
+        lse[r] = total;
+        for (int ch = 0; ch < n_chunks; ++ch) {
+            const double v = lses[(size_t)ch * n_rows + r];
+            if (v == -INFINITY) continue;
+            const double w = exp(v - total);
+            const double *oc = outs + ((size_t)ch * n_rows + r) * d;
+            for (int x = 0; x < d; ++x) out[(size_t)r * d + x] += w * oc[x];
+        }
+    }
+}
+
+/* Number of OpenMP threads a parallel region would use by default. */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
