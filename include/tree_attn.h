@@ -1,0 +1,172 @@
+/*
+ * tree_attn.h -- C ABI of the split tree attention library (libtreeattn.so).
+ *
+ * Split tree attention is the verification attention of EAGLE-style
+ * speculative decoding described in "Efficient Speculative Decoding for Llama
+ * at Scale: Challenges and Solutions" (arXiv 2508.08192; pith.science review,
+ * section "What carries the argument"): the draft tree is flattened into one
+ * sequence of T tokens; attention is computed in two pieces -- every tree
+ * token against the committed prefix with no mask, and the tree tokens among
+ * themselves under the tree mask -- and the two partial results are merged by
+ * log-sum-exp ("merge_attentions", the combination of attention over disjoint
+ * KV chunks named in the review's supporting citations).  The prefix lives in
+ * a paged KV cache ("paged/persistent KV-cache handling for tree attention",
+ * review, Referee Report summary) and is processed split over its length in
+ * the manner of flash-decoding (Dao, Haziza, Massa, Sizov, cited in the
+ * review's reference list).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller.  The library never allocates, frees or
+ *     synchronises; every call only enqueues work on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and returns.
+ *   - bf16 tensors are passed as `const uint16_t *` holding raw bfloat16 bit
+ *     patterns.  All layouts are dense row-major in the order written.
+ *   - `status` (nullable) is a device int32 the caller zeroes beforehand.
+ *     Kernels that detect bad DATA (which the host cannot see without a
+ *     synchronisation) store the first such code there (TREE_ATTN_STATUS_*)
+ *     and leave the outputs unspecified; they never trap.
+ *   - A negative return value means nothing was enqueued.
+ */
+#ifndef TREE_ATTN_H
+#define TREE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TREE_ATTN_API __attribute__((visibility("default")))
+#else
+#define TREE_ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side return codes. */
+#define TREE_ATTN_OK 0
+#define TREE_ATTN_ERR_NULL (-1)       /* a required pointer is NULL                */
+#define TREE_ATTN_ERR_SHAPE (-2)      /* unsupported or inconsistent sizes         */
+#define TREE_ATTN_ERR_ALIGN (-3)      /* a pointer is not suitably aligned         */
+#define TREE_ATTN_ERR_WORKSPACE (-4)  /* workspace NULL, too small or misaligned   */
+#define TREE_ATTN_ERR_CUDA (-5)       /* a CUDA runtime/driver call failed         */
+
+/* Device-side status codes (written to *status). */
+#define TREE_ATTN_STATUS_BAD_PARENT 1   /* parents[i] outside [-1, i)                 */
+#define TREE_ATTN_STATUS_BAD_PAGE 2     /* block_table entry outside [0, num_pages)   */
+#define TREE_ATTN_STATUS_BAD_SEQ_LEN 3  /* seq_lens[b] < 0 or > max_pages_per_seq*P   */
+#define TREE_ATTN_STATUS_TIMEOUT 4      /* an internal pipeline wait gave up           */
+
+/* Limits. */
+#define TREE_ATTN_MAX_T 64
+
+/*
+ * tree_mask_build -- ancestor bitmask of every node of a flattened draft tree.
+ *
+ * Source: "tree mask" of split tree attention (pith.science review,
+ * "What carries the argument"); flattened-draft verification after SpecInfer
+ * (Miao et al., verdict record supporting_citations).
+ *
+ *   parents   int32 [T], parents[i] in {-1} U [0, i): the tree in topological
+ *             order; -1 marks a root (several roots form a forest).
+ *   T         1 .. 64.
+ *   mask_out  uint64 [T]: bit j of mask_out[i] is set iff j == i or node j is
+ *             an ancestor of node i; bits >= T are zero.
+ *   status    nullable; TREE_ATTN_STATUS_BAD_PARENT if a parent is invalid
+ *             (mask_out then unspecified).
+ *
+ * One warp, pointer jumping over log2(T) rounds.  Returns TREE_ATTN_OK,
+ * TREE_ATTN_ERR_NULL, TREE_ATTN_ERR_SHAPE, TREE_ATTN_ERR_ALIGN (mask_out not
+ * 8-byte aligned) or TREE_ATTN_ERR_CUDA.
+ */
+TREE_ATTN_API int tree_mask_build(const int32_t *parents, int T, uint64_t *mask_out,
+                                  int32_t *status, void *stream);
+
+/*
+ * tree_attn_workspace_size -- bytes of device scratch tree_attn_verify needs
+ * for these sizes on the CURRENT device (the count depends on its SM count).
+ * Holds the per-split partial results (m, l, acc) of the prefix pass.
+ * max_seq_len is accepted for interface stability and does not change the
+ * result.  Returns 0 for unsupported sizes.
+ */
+TREE_ATTN_API size_t tree_attn_workspace_size(int B, int Hq, int Hkv, int d, int T,
+                                              int max_seq_len, int page_size);
+
+/*
+ * tree_attn_verify -- split tree attention for one layer.
+ *
+ * For every sequence b, tree node i and query head h (KV head hk = h / G,
+ * G = Hq / Hkv):
+ *   keys  = the seq_lens[b] committed prefix tokens (no mask) plus the tree
+ *           tokens j with bit j of mask[i] set,
+ *   s     = softmax_scale * <q[b][i][h], key>,
+ *   out[b][i][h] = softmax(s) . values   (bf16, round to nearest even),
+ *   lse[b][i][h] = natural-log log-sum-exp of s (fp32).
+ * Computed as (1) a prefix pass split over the KV length, (2) a suffix pass
+ * over the tree keys under the mask, (3) a log-sum-exp merge of all partial
+ * results.
+ *
+ *   q            bf16 [B][T][Hq][d]
+ *   k_pages,
+ *   v_pages      bf16 [num_pages][Hkv][page_size][d]; the slots of a page
+ *                beyond a sequence's length are never used in results.
+ *   block_table  int32 [B][max_pages_per_seq]: physical page of logical page
+ *                p/page_size of sequence b; entries past the sequence's
+ *                last page are ignored.
+ *   seq_lens     int32 [B]: committed prefix length (0 allowed).
+ *   tree_k,
+ *   tree_v       bf16 [B][T][Hkv][d]: the draft tokens' keys and values.
+ *   mask         uint64 [T] (as built by tree_mask_build), shared by all B.
+ *   out          bf16 [B][T][Hq][d];  lse  fp32 [B][T][Hq].
+ *   Sizes: B >= 0 (B = 0 enqueues nothing), 1 <= T <= 64, Hq % Hkv == 0,
+ *          d in {64, 128}, page_size in {16, 32, 64, 128},
+ *          max_pages_per_seq >= 1, num_pages >= 1,
+ *          num_pages*Hkv*page_size < 2^31.
+ *   workspace    device scratch of at least tree_attn_workspace_size(...)
+ *                bytes, 256-byte aligned; contents need no initialisation and
+ *                are garbage afterwards.  Calls that share a workspace must
+ *                not overlap in time.
+ *   status       nullable device int32 (see above).
+ *
+ * Alignment: q, k_pages, v_pages, tree_k, tree_v, out must be 16-byte
+ * aligned; block_table, seq_lens, lse 4-byte; mask 8-byte.
+ * Returns TREE_ATTN_OK or a negative TREE_ATTN_ERR_* code.
+ */
+TREE_ATTN_API int tree_attn_verify(const uint16_t *q, const uint16_t *k_pages,
+                                   const uint16_t *v_pages, const int32_t *block_table,
+                                   int max_pages_per_seq, const int32_t *seq_lens,
+                                   const uint16_t *tree_k, const uint16_t *tree_v,
+                                   const uint64_t *mask, uint16_t *out, float *lse, int B, int Hq,
+                                   int Hkv, int d, int T, int page_size, int num_pages,
+                                   float softmax_scale, void *workspace, size_t workspace_bytes,
+                                   int32_t *status, void *stream);
+
+/*
+ * tree_attn_verify_ctas -- tree_attn_verify with an explicit number of
+ * prefix-pass CTAs (each CTA takes an equal share of the prefix work, so this
+ * is the split count).  n_ctas <= 0 selects the default (one per SM).  The
+ * workspace must then be sized by tree_attn_workspace_size_ctas with the same
+ * n_ctas.  Results differ from the default only by fp32 reassociation.
+ */
+TREE_ATTN_API int tree_attn_verify_ctas(const uint16_t *q, const uint16_t *k_pages,
+                                        const uint16_t *v_pages, const int32_t *block_table,
+                                        int max_pages_per_seq, const int32_t *seq_lens,
+                                        const uint16_t *tree_k, const uint16_t *tree_v,
+                                        const uint64_t *mask, uint16_t *out, float *lse, int B,
+                                        int Hq, int Hkv, int d, int T, int page_size,
+                                        int num_pages, float softmax_scale, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream,
+                                        int n_ctas);
+
+TREE_ATTN_API size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T,
+                                                   int page_size, int n_ctas);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+TREE_ATTN_API int tree_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H */

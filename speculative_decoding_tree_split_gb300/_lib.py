@@ -1,0 +1,195 @@
+"""ctypes binding of libtreeattn.so (C ABI declared in include/tree_attn.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype and
+contiguity, then their data pointers, the sizes and the current CUDA stream
+are handed to the library.  Every step of split tree attention runs in the
+library's kernels.  There is no fallback: if the library is missing or a
+tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtreeattn.so")
+
+# Host-side return codes (include/tree_attn.h).
+ERRORS = {
+    -1: "null pointer",
+    -2: "unsupported or inconsistent sizes",
+    -3: "misaligned pointer",
+    -4: "workspace missing, too small or misaligned",
+    -5: "CUDA error",
+}
+STATUS_BAD_PARENT = 1
+STATUS_BAD_PAGE = 2
+STATUS_BAD_SEQ_LEN = 3
+STATUS_TIMEOUT = 4
+MAX_T = 64
+
+EXPORTED = (
+    "tree_mask_build",
+    "tree_attn_workspace_size",
+    "tree_attn_verify",
+    "tree_attn_verify_ctas",
+    "tree_attn_workspace_size_ctas",
+    "tree_attn_version",
+)
+
+
+class TreeAttnError(RuntimeError):
+    """A negative return code from the C ABI."""
+
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code}: {ERRORS.get(code, 'unknown error')}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtreeattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with speculative_decoding_tree_split_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    lib.tree_mask_build.argtypes = [vp, i32, vp, vp, vp]
+    lib.tree_mask_build.restype = i32
+    lib.tree_attn_workspace_size.argtypes = [i32] * 7
+    lib.tree_attn_workspace_size.restype = sz
+    lib.tree_attn_workspace_size_ctas.argtypes = [i32] * 7
+    lib.tree_attn_workspace_size_ctas.restype = sz
+    verify_args = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                   i32, f32, vp, sz, vp, vp]
+    lib.tree_attn_verify.argtypes = verify_args
+    lib.tree_attn_verify.restype = i32
+    lib.tree_attn_verify_ctas.argtypes = verify_args + [i32]
+    lib.tree_attn_verify_ctas.restype = i32
+    lib.tree_attn_version.argtypes = []
+    lib.tree_attn_version.restype = i32
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtypes, ndim: Optional[int] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+
+
+_BITS64 = (torch.int64, getattr(torch, "uint64", torch.int64))
+
+
+def mask_build(parents: torch.Tensor, mask_out: Optional[torch.Tensor] = None,
+               status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Ancestor-or-self bitmask per node of a flattened draft tree.
+
+    parents: int32 [T] on the GPU.  Returns int64 [T] holding the uint64 bits.
+    """
+    _check(parents, "parents", (torch.int32,), 1)
+    T = parents.shape[0]
+    if mask_out is None:
+        mask_out = torch.empty(T, dtype=torch.int64, device=parents.device)
+    _check(mask_out, "mask_out", _BITS64, 1)
+    if status is not None:
+        _check(status, "status", (torch.int32,))
+    rc = load().tree_mask_build(_ptr(parents), T, _ptr(mask_out), _ptr(status),
+                                _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_mask_build", rc)
+    return mask_out
+
+
+def workspace_size(B: int, Hq: int, Hkv: int, d: int, T: int, max_seq_len: int, page_size: int,
+                   n_ctas: int = 0) -> int:
+    """Workspace bytes tree_attn_verify needs on the current device."""
+    if n_ctas:
+        return int(load().tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, page_size, n_ctas))
+    return int(load().tree_attn_workspace_size(B, Hq, Hkv, d, T, max_seq_len, page_size))
+
+
+def verify(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+           block_table: torch.Tensor, seq_lens: torch.Tensor, tree_k: torch.Tensor,
+           tree_v: torch.Tensor, mask: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+           status: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+           stream=None, n_ctas: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split tree attention for one layer (see tree_attn_verify in the header).
+
+    q [B][T][Hq][d] bf16; k_pages/v_pages [num_pages][Hkv][P][d] bf16;
+    block_table [B][max_pages] int32; seq_lens [B] int32; tree_k/tree_v
+    [B][T][Hkv][d] bf16; mask [T] int64/uint64 bits.  Returns (out, lse).
+    """
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 4)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(tree_k, "tree_k", bf, 4)
+    _check(tree_v, "tree_v", bf, 4)
+    _check(mask, "mask", _BITS64, 1)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, d2 = k_pages.shape
+    if (d2 != d or tuple(v_pages.shape) != tuple(k_pages.shape)
+            or tuple(tree_k.shape) != (B, T, Hkv, d) or tuple(tree_v.shape) != (B, T, Hkv, d)
+            or block_table.shape[0] != B or seq_lens.shape[0] != B or mask.shape[0] != T):
+        raise ValueError("inconsistent tensor shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    _check(out, "out", bf, 4)
+    _check(lse, "lse", (torch.float32,), 3)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, d, T, 0, P, n_ctas)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", (torch.uint8,))
+    if status is not None:
+        _check(status, "status", (torch.int32,))
+    lib = load()
+    args = [_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), _ptr(tree_k), _ptr(tree_v), _ptr(mask), _ptr(out), _ptr(lse),
+            B, Hq, Hkv, d, T, P, num_pages, float(softmax_scale), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(status), _stream_handle(stream)]
+    if n_ctas:
+        rc = lib.tree_attn_verify_ctas(*args, int(n_ctas))
+    else:
+        rc = lib.tree_attn_verify(*args)
+    if rc != 0:
+        raise TreeAttnError("tree_attn_verify", rc)
+    return out, lse
+
+
+def version() -> int:
+    return int(load().tree_attn_version())

@@ -1,0 +1,909 @@
+// kernels.cu -- sm_103a device code of split tree attention.
+//
+//   tree_mask_kernel     ancestor bitmask per tree node (pointer jumping).
+//   prefix_pass_kernel   persistent, warp-specialised flash-decoding prefix
+//                        pass over the paged KV cache: TMA -> shared memory
+//                        ring, S = Q.K^T and O += P.V on tcgen05 tensor cores
+//                        with fp32 accumulators in TMEM, online softmax in
+//                        registers; writes one (m, l, acc) partial per
+//                        segment of its share of the work line.
+//   suffix_merge_kernel  tree-masked suffix pass (T <= 64 keys, SIMT) and
+//                        log-sum-exp merge of every partial into out / lse.
+//
+// Method: split tree attention ("Efficient Speculative Decoding for Llama at
+// Scale", pith.science review, "What carries the argument"): prefix attention
+// needs no mask, tree attention needs the tree mask, and merge_attentions
+// joins the two (verdict record, supporting_citations: attention over
+// disjoint KV chunks, Hydragen).  The prefix pass is split over the KV length
+// as in flash-decoding (Dao, Haziza, Massa, Sizov; review reference list).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/tree_attn.h"
+#include "kernels.cuh"
+#include "layout.h"
+#include "ptx.cuh"
+
+namespace treeattn {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+    if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ===========================================================================
+// Tree mask: node i sees itself and its ancestors.  One warp; lane l owns
+// nodes l and l + 32.  Pointer jumping: after round k, anc[i] holds every
+// node at distance < 2^k above i and jump[i] is the 2^k-th ancestor.  Six
+// rounds cover any depth <= 64.
+// ===========================================================================
+__device__ __forceinline__ uint64_t pick64(uint64_t lo, uint64_t hi, int node) {
+    const uint64_t a = __shfl_sync(kFull, lo, node & 31);
+    const uint64_t b = __shfl_sync(kFull, hi, node & 31);
+    return node < 32 ? a : b;
+}
+
+__device__ __forceinline__ int pick32(int lo, int hi, int node) {
+    const int a = __shfl_sync(kFull, lo, node & 31);
+    const int b = __shfl_sync(kFull, hi, node & 31);
+    return node < 32 ? a : b;
+}
+
+__global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
+                                                       uint64_t* __restrict__ mask,
+                                                       int32_t* status) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+    const int lane = threadIdx.x;
+    int jump[2];
+    uint64_t anc[2];
+    bool bad = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        int p = -1;
+        if (i < T) {
+            p = parents[i];
+            if (p < -1 || p >= i) {
+                bad = true;
+                p = -1;  // treat as a root so the rest stays well defined
+            }
+        }
+        jump[h] = p;
+        anc[h] = (i < T) ? (1ull << i) : 0ull;
+    }
+    if (__any_sync(kFull, bad) && lane == 0) report(status, TREE_ATTN_STATUS_BAD_PARENT);
+#pragma unroll
+    for (int round = 0; round < 6; ++round) {
+        uint64_t na[2];
+        int nj[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = jump[h] < 0 ? 0 : jump[h];
+            const uint64_t aj = pick64(anc[0], anc[1], j);
+            const int jj = pick32(jump[0], jump[1], j);
+            na[h] = jump[h] < 0 ? anc[h] : (anc[h] | aj);
+            nj[h] = jump[h] < 0 ? -1 : jj;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            anc[h] = na[h];
+            jump[h] = nj[h];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        if (i < T) mask[i] = anc[h];
+    }
+}
+
+// ===========================================================================
+// Prefix pass
+// ===========================================================================
+template <int D>
+struct PrefixShape {
+    static constexpr int DH = D / 64;                       // 128-byte d-halves
+    static constexpr int Q_BYTES = kRows * D * 2;           // Q tile, DH atom columns
+    static constexpr int QATOM_BYTES = kRows * 128;         // one atom column of Q / P
+    static constexpr int PBUF_BYTES = kRows * kChunk * 2;   // P (bf16) of one chunk
+    static constexpr int HALF_BYTES = kChunk * 128;         // 64 keys x 64 d of K or V
+    static constexpr int TILE_BYTES = DH * HALF_BYTES;      // K (or V) of one chunk
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int NS = (D == 128) ? 4 : 8;           // ring depth
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;
+    static constexpr int OFF_STAGE = OFF_P + 2 * PBUF_BYTES;
+    static constexpr int OFF_BAR = OFF_STAGE + NS * STAGE_BYTES;
+    // barrier indices
+    static constexpr int KV_FULL = 0;
+    static constexpr int KV_EMPTY = NS;
+    static constexpr int S_FULL = 2 * NS;
+    static constexpr int S_FREE = 2 * NS + 2;
+    static constexpr int P_FULL = 2 * NS + 4;
+    static constexpr int P_FREE = 2 * NS + 6;
+    static constexpr int O_FULL = 2 * NS + 8;
+    static constexpr int O_FREE = 2 * NS + 10;
+    static constexpr int Q_FULL = 2 * NS + 12;
+    static constexpr int DRAIN = 2 * NS + 13;
+    static constexpr int NBAR = 2 * NS + 14;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    // TMEM columns: O[2] at [0, 2D), S[2] at [2D, 2D + 2*64).
+    static constexpr int TM_O = 0;
+    static constexpr int TM_S = 2 * D;
+    static constexpr int TMEM_COLS = (2 * D + 2 * kChunk) > 256 ? 512 : 256;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
+};
+
+struct PrefixMisc {
+    long long W, x0, x1, base0;
+    int b0;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct PrefixArgs {
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const uint16_t* q;
+    float* ws;
+    int32_t* status;
+    int B, Hq, Hkv, G, T, M, RB, P, max_pages, num_pages, n_ctas;
+    float scale_log2;
+};
+
+__device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long n = __shfl_up_sync(kFull, v, off);
+        if (lane >= off) v += n;
+    }
+    return v;
+}
+
+// Total work W and this CTA's starting sequence / base (warp 0, all lanes).
+__device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
+    const int upb = a.Hkv * a.RB;
+    long long tot = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        int n = 0;
+        if (b < a.B) {
+            bool bad;
+            n = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+            if (bad && blockIdx.x == 0) report(a.status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
+        }
+        tot += __reduce_add_sync(kFull, n);
+    }
+    const long long W = tot * upb;
+    const long long x0 = cta_start(blockIdx.x, W, a.n_ctas);
+    const long long x1 = cta_start(blockIdx.x + 1, W, a.n_ctas);
+    int b_start = 0;
+    long long base0 = 0;
+    if (x0 < x1) {
+        long long run = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int b = b0 + lane;
+            long long n = 0;
+            if (b < a.B) {
+                bool bad;
+                n = static_cast<long long>(upb) *
+                    chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+            }
+            const long long incl = warp_incl_scan(n, lane);
+            const long long excl = incl - n;
+            const bool hit = (b < a.B) && (run + excl <= x0) && (x0 < run + incl);
+            const unsigned m = __ballot_sync(kFull, hit);
+            if (m != 0) {
+                const int src = __ffs(m) - 1;
+                b_start = b0 + src;
+                base0 = run + __shfl_sync(kFull, excl, src);
+                break;
+            }
+            run += __shfl_sync(kFull, incl, 31);
+        }
+    }
+    if (lane == 0) {
+        misc->W = W;
+        misc->x0 = x0;
+        misc->x1 = x1;
+        misc->b0 = b_start;
+        misc->base0 = base0;
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const PrefixArgs a) {
+    using S = PrefixShape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sb = raw_addr + pad;  // 1024-aligned shared address of the layout
+    PrefixMisc* misc = reinterpret_cast<PrefixMisc*>(smem + S::OFF_MISC);
+    volatile int* abort_flag = &misc->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sb + S::OFF_BAR + 8u * i; };
+
+    // ---------------- prologue (overlaps the previous kernel under PDL)
+    if (warp == 4 && lane == 0) {
+        for (int s = 0; s < S::NS; ++s) {
+            ptx::mbar_init(bar(S::KV_FULL + s), 1);
+            ptx::mbar_init(bar(S::KV_EMPTY + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar(S::S_FULL + i), 1);
+            ptx::mbar_init(bar(S::S_FREE + i), 4);
+            ptx::mbar_init(bar(S::P_FULL + i), 4);
+            ptx::mbar_init(bar(S::P_FREE + i), 1);
+            ptx::mbar_init(bar(S::O_FULL + i), 1);
+            ptx::mbar_init(bar(S::O_FREE + i), 4);
+        }
+        ptx::mbar_init(bar(S::Q_FULL), 4);
+        ptx::mbar_init(bar(S::DRAIN), 1);
+        misc->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 5) {
+        ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), S::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // Inputs may come from the kernel before us in the stream.
+    ptx::grid_dep_wait();
+    if (warp == 0) compute_plan(a, lane, misc);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    ptx::grid_dep_launch();
+    const uint32_t tmem = misc->tmem_base;
+    const int upb = a.Hkv * a.RB;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        report(a.status, TREE_ATTN_STATUS_TIMEOUT);
+    };
+
+    if (warp == 4) {
+        // ================= TMA producer (one thread)
+        if (lane == 0) {
+            Walker w;
+            w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
+                   misc->x1);
+            const uint64_t pol = ptx::policy_evict_first();
+            const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
+            const int nsub = kChunk / Pb;                // boxes per chunk (pages < 64 tokens)
+            uint32_t jj = 0;
+            bool ok = true;
+            Segment sg;
+            while (ok && w.next(sg)) {
+                bool bad;
+                const int L = clamp_seq_len(a.seq_lens[sg.b], a.P, a.max_pages, bad);
+                const int npages = (L + a.P - 1) / a.P;
+                const int32_t* bt = a.block_table + static_cast<size_t>(sg.b) * a.max_pages;
+                for (int ch = sg.chunk_begin; ch < sg.chunk_end; ++ch, ++jj) {
+                    const int s = jj % S::NS;
+                    if (jj >= S::NS &&
+                        !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    int ys[4];
+                    int rows[4];
+                    int nl = 0;
+                    for (int i = 0; i < nsub; ++i) {
+                        const int tok = ch * kChunk + i * Pb;
+                        const int lp = tok / a.P;
+                        if (lp >= npages) break;
+                        const int pid = bt[lp];
+                        if (pid < 0 || pid >= a.num_pages) {
+                            report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
+                            continue;
+                        }
+                        ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok % a.P);
+                        rows[nl] = i * Pb;
+                        ++nl;
+                    }
+                    const uint32_t fb = bar(S::KV_FULL + s);
+                    const uint32_t bytes = static_cast<uint32_t>(nl * Pb * 128 * S::DH * 2);
+                    if (bytes != 0) {
+                        ptx::mbar_arrive_expect_tx(fb, bytes);
+                    } else {
+                        ptx::mbar_arrive(fb);
+                    }
+                    const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
+                    const uint32_t vst = kst + S::TILE_BYTES;
+                    for (int l = 0; l < nl; ++l) {
+#pragma unroll
+                        for (int h = 0; h < S::DH; ++h) {
+                            ptx::tma_load_2d(kst + h * S::HALF_BYTES + rows[l] * 128, &tm_k, h * 64,
+                                             ys[l], fb, pol);
+                            ptx::tma_load_2d(vst + h * S::HALF_BYTES + rows[l] * 128, &tm_v, h * 64,
+                                             ys[l], fb, pol);
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy still in flight land before the CTA exits.
+                const uint32_t first = jj > S::NS ? jj - S::NS : 0;
+                for (uint32_t j = first; j < jj; ++j)
+                    (void)ptx::mbar_wait(bar(S::KV_FULL + j % S::NS), (j / S::NS) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ================= MMA issuer (one thread)
+        if (lane == 0) {
+            Walker w;
+            w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
+                   misc->x1);
+            const uint32_t idesc_qk = idesc_bf16_f32(kRows, kChunk, false, false);
+            const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
+            uint32_t jj = 0, kk = 0;
+            bool ok = true;
+            Segment sg;
+            // O[kk&1] += P[j&1] . V[stage of j]
+            auto issue_pv = [&](uint32_t j, bool first) -> bool {
+                if (!ptx::mbar_wait(bar(S::P_FULL + (j & 1)), (j >> 1) & 1)) return false;
+                if (first && kk >= 2 &&
+                    !ptx::mbar_wait(bar(S::O_FREE + (kk & 1)), ((kk >> 1) - 1) & 1))
+                    return false;
+                ptx::tc_fence_after();
+                const uint32_t vst =
+                    sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
+                const uint32_t pst = sb + S::OFF_P + (j & 1) * S::PBUF_BYTES;
+                const uint32_t d_o = tmem + S::TM_O + (kk & 1) * D;
+#pragma unroll
+                for (int k = 0; k < kChunk / 16; ++k) {
+                    const uint64_t ad = smem_desc_sw128(pst + k * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(vst + k * 16 * 128, S::HALF_BYTES, 1024);
+                    ptx::mma_bf16(d_o, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+                }
+                ptx::mma_commit(bar(S::KV_EMPTY + j % S::NS));
+                ptx::mma_commit(bar(S::P_FREE + (j & 1)));
+                return true;
+            };
+            while (ok && w.next(sg)) {
+                if (!ptx::mbar_wait(bar(S::Q_FULL), kk & 1)) {
+                    fail();
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int n = sg.chunk_end - sg.chunk_begin;
+                for (int p = 0; p < n; ++p, ++jj) {
+                    const int s = jj % S::NS;
+                    if (!ptx::mbar_wait(bar(S::KV_FULL + s), (jj / S::NS) & 1) ||
+                        (jj >= 2 &&
+                         !ptx::mbar_wait(bar(S::S_FREE + (jj & 1)), ((jj >> 1) - 1) & 1)) ||
+                        *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
+                    const uint32_t d_s = tmem + S::TM_S + (jj & 1) * kChunk;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t ad = smem_desc_sw128(
+                            sb + S::OFF_Q + (k >> 2) * S::QATOM_BYTES + (k & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(
+                            kst + (k >> 2) * S::HALF_BYTES + (k & 3) * 32, 16, 1024);
+                        ptx::mma_bf16(d_s, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar(S::S_FULL + (jj & 1)));
+                    if (p > 0 && !issue_pv(jj - 1, p == 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) {
+                    fail();
+                    break;
+                }
+                if (!issue_pv(jj - 1, n == 1)) {
+                    fail();
+                    break;
+                }
+                ptx::mma_commit(bar(S::O_FULL + (kk & 1)));
+                ++kk;
+            }
+            // Every MMA issued above must finish before TMEM is released.
+            ptx::mma_commit(bar(S::DRAIN));
+            (void)ptx::mbar_wait(bar(S::DRAIN), 0);
+        }
+    } else {
+        // ================= softmax + epilogue warpgroup (warps 0-3)
+        const int r = threadIdx.x;  // tile row == TMEM lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        Walker w;
+        w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
+               misc->x1);
+        auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+            const bool ok = ptx::mbar_wait(b, parity);
+            const bool all = __all_sync(kFull, ok) && !*abort_flag;
+            if (!ok) fail();
+            return all;
+        };
+        // Stage Q rows of a segment into the swizzled K-major A tile.
+        auto load_q = [&](const Segment& sg) {
+            const int Mrb = min(kRows, a.M - sg.rb * kRows);
+            uint8_t* qs = smem + S::OFF_Q;
+            if (r < Mrb) {
+                const int rr = sg.rb * kRows + r;
+                const int t = rr / a.G, g = rr % a.G;
+                const int h = sg.hk * a.G + g;
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    a.q + ((static_cast<size_t>(sg.b) * a.T + t) * a.Hq + h) * D);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = __ldg(src + c);
+                    *reinterpret_cast<uint4*>(qs + (c >> 3) * S::QATOM_BYTES +
+                                              sw128_offset(r, c & 7)) = v;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                    *reinterpret_cast<uint4*>(qs + (c >> 3) * S::QATOM_BYTES +
+                                              sw128_offset(r, c & 7)) = make_uint4(0, 0, 0, 0);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(S::Q_FULL));
+        };
+
+        uint32_t jj = 0, kk = 0;
+        Segment cur;
+        bool have = w.next(cur);
+        bool ok = true;
+        if (have) load_q(cur);
+        while (ok && have) {
+            const int Mrb = min(kRows, a.M - cur.rb * kRows);
+            const bool row_ok = r < Mrb;
+            const bool warp_any = warp * 32 < Mrb;
+            bool bad;
+            const int L = clamp_seq_len(a.seq_lens[cur.b], a.P, a.max_pages, bad);
+            float m_ref = kNegInf;
+            float l_sum = 0.f;
+            for (int ch = cur.chunk_begin; ch < cur.chunk_end; ++ch, ++jj) {
+                const bool first = ch == cur.chunk_begin;
+                const int n_valid = min(kChunk, L - ch * kChunk);
+                if (!wait_all(bar(S::S_FULL + (jj & 1)), (jj >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                float s[kChunk];
+                if (warp_any) {
+                    const uint32_t ta = lane_base + S::TM_S + (jj & 1) * kChunk;
+                    ptx::tmem_ld32(ta, s);
+                    ptx::tmem_ld32(ta + 32, s + 32);
+                    ptx::tmem_wait_ld();
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(S::S_FREE + (jj & 1)));
+
+                float alpha = 1.f;
+                bool rescale = false;
+                if (row_ok) {
+                    float mx = kNegInf;
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i) {
+                        const float x = (i < n_valid) ? s[i] * a.scale_log2 : kNegInf;
+                        s[i] = x;
+                        mx = fmaxf(mx, x);
+                    }
+                    if (first) {
+                        m_ref = mx;
+                    } else if (mx > m_ref + 8.f) {
+                        // Keep 2^(x - m_ref) <= 2^8: move the reference and
+                        // rescale the running sums.
+                        alpha = ptx::ex2(m_ref - mx);
+                        m_ref = mx;
+                        l_sum *= alpha;
+                        rescale = true;
+                    }
+                    float sum = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i) {
+                        s[i] = ptx::ex2(s[i] - m_ref);
+                        sum += s[i];
+                    }
+                    l_sum += sum;
+                }
+                // P buffer (jj & 1) is free once PV(jj - 2) has completed.
+                if (jj >= 2 && !wait_all(bar(S::P_FREE + (jj & 1)), ((jj >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (row_ok) {
+                    const uint32_t pst = sb + S::OFF_P + (jj & 1) * S::PBUF_BYTES;
+#pragma unroll
+                    for (int c = 0; c < kChunk / 8; ++c) {
+                        st_shared_v4(pst + sw128_offset(r, c), pack_bf16(s[8 * c], s[8 * c + 1]),
+                                     pack_bf16(s[8 * c + 2], s[8 * c + 3]),
+                                     pack_bf16(s[8 * c + 4], s[8 * c + 5]),
+                                     pack_bf16(s[8 * c + 6], s[8 * c + 7]));
+                    }
+                }
+                if (__any_sync(kFull, rescale)) {
+                    // O must hold PV(jj - 1) before it is rescaled in place.
+                    if (!wait_all(bar(S::P_FREE + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t to = lane_base + S::TM_O + (kk & 1) * D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        ptx::tmem_ld32(to + c, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        ptx::tmem_st32(to + c, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+                if (n_valid < kChunk) {
+                    // Slots past the sequence end hold stale data; zero their
+                    // V rows so 0 * garbage cannot reach O.
+                    if (!wait_all(bar(S::KV_FULL + jj % S::NS), (jj / S::NS) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vst =
+                        sb + S::OFF_STAGE + (jj % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
+                    const int items = (kChunk - n_valid) * S::DH * 8;
+                    for (int it = r; it < items; it += 128) {
+                        const int row = n_valid + it / (S::DH * 8);
+                        const int rem = it % (S::DH * 8);
+                        st_shared_v4(vst + (rem >> 3) * S::HALF_BYTES + row * 128 + (rem & 7) * 16,
+                                     0u, 0u, 0u, 0u);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(S::P_FULL + (jj & 1)));
+            }
+            if (!ok) break;
+            // Stage the next segment's Q first so its S MMA overlaps this
+            // epilogue (every S MMA of this segment has completed).
+            Segment nxt;
+            const bool have_next = w.next(nxt);
+            if (have_next) load_q(nxt);
+            if (!wait_all(bar(S::O_FULL + (kk & 1)), (kk >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (warp_any) {
+                float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
+                const uint32_t to = lane_base + S::TM_O + (kk & 1) * D;
+                float4* acc =
+                    reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    float o[32];
+                    ptx::tmem_ld32(to + c, o);
+                    ptx::tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc[c / 4 + i] =
+                                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+                if (row_ok) {
+                    slot[r] = m_ref;
+                    slot[kRows + r] = l_sum;
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(S::O_FREE + (kk & 1)));
+            ++kk;
+            cur = nxt;
+            have = have_next;
+        }
+    }
+
+    // ---------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+}
+
+// ===========================================================================
+// Suffix pass + merge.  One warp per query row; lane l holds elements
+// [l*E, l*E + E) of the head dimension.
+// ===========================================================================
+struct MergeArgs {
+    const uint16_t* q;
+    const uint16_t* tree_k;
+    const uint16_t* tree_v;
+    const uint64_t* mask;
+    const int32_t* seq_lens;
+    const float* ws;
+    uint16_t* out;
+    float* lse;
+    int B, Hq, Hkv, G, T, M, RB, P, max_pages, n_ctas;
+    float scale_log2;
+};
+
+template <int E>
+__device__ __forceinline__ void load_bf16(const uint16_t* p, float* v) {
+    if constexpr (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        v[0] = __uint_as_float(u << 16);
+        v[1] = __uint_as_float(u & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+
+constexpr int kMergeRows = 8;  // rows (warps) per CTA
+
+template <int D>
+__global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const MergeArgs a) {
+    constexpr int E = D / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.x;
+    const int rb = unit % a.RB;
+    const int hk = (unit / a.RB) % a.Hkv;
+    const int b = unit / (a.RB * a.Hkv);
+    const int r = blockIdx.y * kMergeRows + warp;
+    const int rr = rb * kRows + r;
+    const bool active = r < kRows && rr < a.M;
+
+    // ---- suffix: online softmax over the tree keys mask[t] allows.  Reads
+    // only inputs of this call, so it runs before waiting for the prefix pass.
+    float m_s = kNegInf, l_s = 0.f;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    int t = 0, h = 0;
+    if (active) {
+        t = rr / a.G;
+        h = hk * a.G + rr % a.G;
+        float qv[E];
+        load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
+        uint64_t bits = a.mask[t];
+        if (a.T < 64) bits &= (1ull << a.T) - 1ull;
+        while (bits != 0) {
+            const int j = __ffsll(static_cast<long long>(bits)) - 1;
+            bits &= bits - 1;
+            const size_t off = ((static_cast<size_t>(b) * a.T + j) * a.Hkv + hk) * D + lane * E;
+            float kv[E], vv[E];
+            load_bf16<E>(a.tree_k + off, kv);
+            load_bf16<E>(a.tree_v + off, vv);
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
+            const float x = warp_sum(dot) * a.scale_log2;
+            const float mn = fmaxf(m_s, x);
+            const float al = ptx::ex2(m_s - mn);
+            const float p = ptx::ex2(x - mn);
+            l_s = l_s * al + p;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[e], acc[e] * al);
+            m_s = mn;
+        }
+    }
+
+    // ---- partials of the prefix pass
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+    if (!active) return;
+    const int upb = a.Hkv * a.RB;
+    long long W = 0, base_b = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int bb = b0 + lane;
+        int n = 0;
+        if (bb < a.B) {
+            bool bad;
+            n = chunks_of(clamp_seq_len(a.seq_lens[bb], a.P, a.max_pages, bad));
+        }
+        W += __reduce_add_sync(kFull, n);
+        base_b += __reduce_add_sync(kFull, bb < b ? n : 0);
+    }
+    W *= upb;
+    base_b *= upb;
+    bool bad;
+    const int nch = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+    const size_t sf = static_cast<size_t>(slot_floats(D));
+    float mx = m_s;
+    int c_first = 0, c_last = -1;
+    if (nch > 0) {
+        const long long ustart = base_b + static_cast<long long>(unit - b * upb) * nch;
+        c_first = cta_of(ustart, W, a.n_ctas);
+        c_last = cta_of(ustart + nch - 1, W, a.n_ctas);
+        for (int c = c_first + lane; c <= c_last; c += 32)
+            if (cta_has_work(c, W, a.n_ctas)) mx = fmaxf(mx, a.ws[(unit + c) * sf + r]);
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    }
+    uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
+    float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
+    if (mx == kNegInf) {  // no key at all
+#pragma unroll
+        for (int e = 0; e < E; ++e) op[e] = 0;
+        if (lane == 0) *lp = kNegInf;
+        return;
+    }
+    const float w_s = ptx::ex2(m_s - mx);
+    float total = l_s * w_s;
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = acc[e] * w_s;
+    for (int c = c_first; c <= c_last; ++c) {
+        if (!cta_has_work(c, W, a.n_ctas)) continue;
+        const float* slot = a.ws + (unit + c) * sf;
+        const float wc = ptx::ex2(slot[r] - mx);
+        total = fmaf(wc, slot[kRows + r], total);
+        const float* ac = slot + 2 * kRows + static_cast<size_t>(r) * D + lane * E;
+        if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(ac);
+            o[0] = fmaf(wc, v.x, o[0]);
+            o[1] = fmaf(wc, v.y, o[1]);
+            o[2] = fmaf(wc, v.z, o[2]);
+            o[3] = fmaf(wc, v.w, o[3]);
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(ac);
+            o[0] = fmaf(wc, v.x, o[0]);
+            o[1] = fmaf(wc, v.y, o[1]);
+        }
+    }
+    const float inv = 1.f / total;
+    if constexpr (E == 4) {
+        uint2 pk;
+        pk.x = pack_bf16(o[0] * inv, o[1] * inv);
+        pk.y = pack_bf16(o[2] * inv, o[3] * inv);
+        *reinterpret_cast<uint2*>(op) = pk;
+    } else {
+        *reinterpret_cast<uint32_t*>(op) = pack_bf16(o[0] * inv, o[1] * inv);
+    }
+    if (lane == 0) *lp = (mx + log2f(total)) * kLn2;
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int D>
+cudaError_t launch_verify_d(const VerifyArgs& v, const void* tmap_k, const void* tmap_v,
+                            cudaStream_t stream) {
+    using S = PrefixShape<D>;
+    static int configured_for = -1;  // device on which the smem opt-in was applied
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_for != dev) {
+        e = cudaFuncSetAttribute(prefix_pass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_for = dev;
+    }
+    const int G = v.Hq / v.Hkv;
+    const int M = v.T * G;
+    const int RB = (M + kRows - 1) / kRows;
+    PrefixArgs pa;
+    pa.block_table = v.block_table;
+    pa.seq_lens = v.seq_lens;
+    pa.q = v.q;
+    pa.ws = v.ws;
+    pa.status = v.status;
+    pa.B = v.B;
+    pa.Hq = v.Hq;
+    pa.Hkv = v.Hkv;
+    pa.G = G;
+    pa.T = v.T;
+    pa.M = M;
+    pa.RB = RB;
+    pa.P = v.P;
+    pa.max_pages = v.max_pages;
+    pa.num_pages = v.num_pages;
+    pa.n_ctas = v.n_ctas;
+    pa.scale_log2 = v.scale_log2;
+    const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
+    const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
+    e = launch_pdl(prefix_pass_kernel<D>, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv,
+                   pa);
+    if (e != cudaSuccess) return e;
+
+    MergeArgs ma;
+    ma.q = v.q;
+    ma.tree_k = v.tree_k;
+    ma.tree_v = v.tree_v;
+    ma.mask = v.mask;
+    ma.seq_lens = v.seq_lens;
+    ma.ws = v.ws;
+    ma.out = v.out;
+    ma.lse = v.lse;
+    ma.B = v.B;
+    ma.Hq = v.Hq;
+    ma.Hkv = v.Hkv;
+    ma.G = G;
+    ma.T = v.T;
+    ma.M = M;
+    ma.RB = RB;
+    ma.P = v.P;
+    ma.max_pages = v.max_pages;
+    ma.n_ctas = v.n_ctas;
+    ma.scale_log2 = v.scale_log2;
+    const int rows = M < kRows ? M : kRows;
+    const dim3 grid(v.B * v.Hkv * RB, (rows + kMergeRows - 1) / kMergeRows);
+    return launch_pdl(suffix_merge_kernel<D>, grid, dim3(32 * kMergeRows), 0, stream, ma);
+}
+
+}  // namespace
+
+cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int32_t* status,
+                              cudaStream_t stream) {
+    return launch_pdl(tree_mask_kernel, dim3(1), dim3(32), 0, stream, parents, T, mask, status);
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+                          cudaStream_t stream) {
+    if (a.d == 128) return launch_verify_d<128>(a, tmap_k, tmap_v, stream);
+    return launch_verify_d<64>(a, tmap_k, tmap_v, stream);
+}
+
+}  // namespace treeattn

@@ -1,0 +1,38 @@
+// kernels.cuh -- launch interface between the C-ABI layer (tree_attn.cu) and
+// the device code (kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace treeattn {
+
+struct VerifyArgs {
+    const uint16_t* q;
+    const uint16_t* k_pages;
+    const uint16_t* v_pages;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const uint16_t* tree_k;
+    const uint16_t* tree_v;
+    const uint64_t* mask;
+    uint16_t* out;
+    float* lse;
+    float* ws;
+    int32_t* status;
+    int B, Hq, Hkv, d, T, P, max_pages, num_pages;
+    int n_ctas;
+    float scale_log2;
+};
+
+// Enqueue the mask builder (one warp).  Returns a cudaError_t.
+cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int32_t* status,
+                              cudaStream_t stream);
+
+// Enqueue the prefix pass and the suffix + merge pass.  `tmap_k`/`tmap_v`
+// point at encoded CUtensorMap objects (host memory, copied into the launch).
+cudaError_t launch_verify(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+                          cudaStream_t stream);
+
+}  // namespace treeattn

@@ -1,0 +1,200 @@
+// layout.h -- plain C++ helpers shared by the host code, the kernels and the
+// CPU unit tests of this library (compiles with g++ or nvcc):
+//   * tcgen05 shared-memory and instruction descriptors,
+//   * the prefix-pass work partition (the "work line") and the slot index of
+//     every partial result.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define TA_HD __host__ __device__ __forceinline__
+#else
+#define TA_HD inline
+#endif
+
+namespace treeattn {
+
+// Prefix keys are processed in chunks of 64 tokens: one 128-byte swizzle atom
+// of bf16 keys, the N of the S = Q.K^T MMA and the K of the P.V MMA.
+constexpr int kChunk = 64;
+// Query rows per CTA tile (the M of both MMAs, one TMEM lane per row).
+constexpr int kRows = 128;
+
+// ---------------------------------------------------------------------------
+// tcgen05 descriptors
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor, 128-byte swizzle:
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-47  descriptor version (1 on sm_100-class tensor cores)
+//   bits 49-51  base offset (0: every tile starts 1024-byte aligned)
+//   bit  52     leading-dimension offset mode (0: relative)
+//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+// K-major operands: rows of 128 B (64 bf16 along K), 8-row groups SBO apart;
+// LBO unused.  MN-major operands: 64 elements along M/N per 128-B row, LBO
+// between such 64-element blocks, SBO between groups of 8 rows along K.
+TA_HD uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    return static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) |
+           (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor for tcgen05.mma kind::f16 with bf16 A and B and an
+// fp32 accumulator:
+//   bits 4-5 D format (1 = f32), bits 7-9 A format (1 = bf16),
+//   bits 10-12 B format (1 = bf16), bit 15 A major (1 = MN-major),
+//   bit 16 B major (1 = MN-major), bits 17-22 N >> 3, bits 24-28 M >> 4.
+TA_HD uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+           ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a K-major
+// 128-byte-swizzled tile whose rows are 128 B long (the layout TMA writes
+// with CU_TENSOR_MAP_SWIZZLE_128B and the tensor core reads).
+TA_HD uint32_t sw128_offset(uint32_t r, uint32_t c) {
+    return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// Work line of the prefix pass
+// ---------------------------------------------------------------------------
+// A "unit" is (sequence b, KV head hk, row block rb); units are numbered
+// u = (b * Hkv + hk) * RB + rb.  Unit u owns chunks(b) = ceil(L_b / 64) steps
+// of work.  Laying all units' steps end to end gives the work line of length
+// W; CTA c of C takes the steps [start(c), start(c+1)), start(c) = c*W/C.
+// The piece of unit u handled by CTA c is a "segment"; its partial result
+// (m, l, acc) goes to slot u + c, which is unique because moving along the
+// work line from one segment to the next increases u, c or both.  At most
+// U + C - 1 slots are used.
+
+// Committed prefix length actually used for sequence b: clamped to
+// [0, max_pages*P]; `bad` is set when clamping was needed.
+TA_HD int clamp_seq_len(int32_t L, int P, int max_pages, bool& bad) {
+    const long long cap = static_cast<long long>(max_pages) * P;
+    bad = false;
+    if (L < 0) {
+        bad = true;
+        return 0;
+    }
+    if (L > cap) {
+        bad = true;
+        return static_cast<int>(cap);
+    }
+    return L;
+}
+
+TA_HD int chunks_of(int L) { return (L + kChunk - 1) / kChunk; }
+
+TA_HD long long cta_start(int c, long long W, int C) {
+    return static_cast<long long>(c) * W / C;
+}
+
+// The CTA whose range holds work-line position x (0 <= x < W).
+TA_HD int cta_of(long long x, long long W, int C) {
+    return static_cast<int>((x * C + C - 1) / W);
+}
+
+// True when CTA c has work (an empty range happens when W < C).  The merge
+// side skips empty CTAs between a unit's first and last CTA: they wrote no
+// partial.
+TA_HD bool cta_has_work(int c, long long W, int C) {
+    return cta_start(c, W, C) < cta_start(c + 1, W, C);
+}
+
+struct Segment {
+    int b, hk, rb, unit;
+    int chunk_begin, chunk_end;  // chunk indices within sequence b
+};
+
+// Walks the segments of one CTA's range in order.  `seq_lens` is read
+// directly (device or host memory, depending on who runs it).
+struct Walker {
+    const int32_t* seq_lens;
+    int B, P, max_pages, units_per_b, RB;
+    int b;           // current sequence
+    long long base;  // work-line position of sequence b's first unit
+    int nch;         // chunks per unit of sequence b
+    long long x, x1; // current position and end of this CTA's range
+
+    TA_HD int chunks_b(int bb) const {
+        bool bad;
+        return chunks_of(clamp_seq_len(seq_lens[bb], P, max_pages, bad));
+    }
+
+    TA_HD void init(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
+                    long long base0, long long x0, long long x1_) {
+        seq_lens = sl;
+        B = B_;
+        P = P_;
+        max_pages = maxp;
+        units_per_b = upb;
+        RB = RB_;
+        b = b0;
+        base = base0;
+        x = x0;
+        x1 = x1_;
+        nch = (x0 < x1_) ? chunks_b(b0) : 0;
+    }
+
+    TA_HD bool next(Segment& s) {
+        if (x >= x1) return false;
+        while (x >= base + static_cast<long long>(units_per_b) * nch) {
+            base += static_cast<long long>(units_per_b) * nch;
+            ++b;
+            nch = chunks_b(b);
+        }
+        const long long off = x - base;
+        const int urel = static_cast<int>(off / nch);
+        const int ch = static_cast<int>(off % nch);
+        const long long uend = base + static_cast<long long>(urel + 1) * nch;
+        const long long e = x1 < uend ? x1 : uend;
+        s.b = b;
+        s.hk = urel / RB;
+        s.rb = urel % RB;
+        s.unit = b * units_per_b + urel;
+        s.chunk_begin = ch;
+        s.chunk_end = ch + static_cast<int>(e - x);
+        x = e;
+        return true;
+    }
+};
+
+// Serial form of the per-CTA start search (host code and tests): total work
+// W and, for CTA c, the sequence b0 holding start(c) and that sequence's
+// work-line base.  The kernels compute the same values with warp scans.
+inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, int upb, int C,
+                        int c, long long& W, int& b0, long long& base0, long long& x0,
+                        long long& x1) {
+    long long tot = 0;
+    for (int b = 0; b < B; ++b) {
+        bool bad;
+        tot += chunks_of(clamp_seq_len(seq_lens[b], P, max_pages, bad));
+    }
+    W = tot * upb;
+    x0 = cta_start(c, W, C);
+    x1 = cta_start(c + 1, W, C);
+    b0 = 0;
+    base0 = 0;
+    long long run = 0;
+    for (int b = 0; b < B; ++b) {
+        bool bad;
+        const long long w = static_cast<long long>(upb) *
+                            chunks_of(clamp_seq_len(seq_lens[b], P, max_pages, bad));
+        if (x0 < run + w) {
+            b0 = b;
+            base0 = run;
+            return;
+        }
+        run += w;
+    }
+}
+
+// Partial-result slot layout: m[kRows] | l[kRows] | acc[kRows][d] (fp32).
+TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>(kRows) * d; }
+
+}  // namespace treeattn

@@ -1,0 +1,181 @@
+// tree_attn.cu -- the C ABI (include/tree_attn.h): argument checks, workspace
+// sizing, TMA tensor-map encoding and kernel launches.  No allocation, no
+// synchronisation: every call only enqueues work on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/tree_attn.h"
+#include "kernels.cuh"
+#include "layout.h"
+
+using namespace treeattn;
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool shape_ok(int B, int Hq, int Hkv, int d, int T, int P) {
+    if (B < 0 || T < 1 || T > TREE_ATTN_MAX_T || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return false;
+    if (d != 64 && d != 128) return false;
+    if (P != 16 && P != 32 && P != 64 && P != 128) return false;
+    return true;
+}
+
+size_t ws_bytes(int B, int Hq, int Hkv, int d, int T, int n_ctas) {
+    const long long G = Hq / Hkv;
+    const long long M = static_cast<long long>(T) * G;
+    const long long RB = (M + kRows - 1) / kRows;
+    const long long units = static_cast<long long>(B) * Hkv * RB;
+    const long long slots = units + n_ctas;
+    const size_t bytes = static_cast<size_t>(slots) * slot_floats(d) * sizeof(float);
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+// Row-major [rows][d] bf16 view of a paged cache, boxes of `box_rows` x 64.
+bool encode_pages(CUtensorMap* map, const void* base, long long rows, int d, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tree_attn_version(void) { return 10000; }
+
+int tree_mask_build(const int32_t* parents, int T, uint64_t* mask_out, int32_t* status,
+                    void* stream) {
+    if (parents == nullptr || mask_out == nullptr) return TREE_ATTN_ERR_NULL;
+    if (T < 1 || T > TREE_ATTN_MAX_T) return TREE_ATTN_ERR_SHAPE;
+    if (!aligned(parents, 4) || !aligned(mask_out, 8) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    const cudaError_t e =
+        launch_mask_build(parents, T, mask_out, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T, int page_size,
+                                     int n_ctas) {
+    if (!shape_ok(B, Hq, Hkv, d, T, page_size)) return 0;
+    if (n_ctas <= 0) n_ctas = sm_count();
+    if (n_ctas <= 0) return 0;
+    return ws_bytes(B, Hq, Hkv, d, T, n_ctas);
+}
+
+size_t tree_attn_workspace_size(int B, int Hq, int Hkv, int d, int T, int max_seq_len,
+                                int page_size) {
+    (void)max_seq_len;
+    return tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, page_size, 0);
+}
+
+int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                          const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, const uint16_t* tree_k,
+                          const uint16_t* tree_v, const uint64_t* mask, uint16_t* out,
+                          float* lse, int B, int Hq, int Hkv, int d, int T, int page_size,
+                          int num_pages, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream, int n_ctas) {
+    if (!shape_ok(B, Hq, Hkv, d, T, page_size) || max_pages_per_seq < 1 || num_pages < 1 ||
+        !std::isfinite(softmax_scale))
+        return TREE_ATTN_ERR_SHAPE;
+    if (static_cast<long long>(num_pages) * Hkv * page_size >= (1LL << 31))
+        return TREE_ATTN_ERR_SHAPE;
+    if (B == 0) return TREE_ATTN_OK;
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !tree_k || !tree_v || !mask ||
+        !out || !lse)
+        return TREE_ATTN_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(tree_k, 16) ||
+        !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    if (n_ctas <= 0) n_ctas = sm_count();
+    if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
+        return TREE_ATTN_ERR_WORKSPACE;
+
+    const long long rows = static_cast<long long>(num_pages) * Hkv * page_size;
+    const int box_rows = page_size < kChunk ? page_size : kChunk;
+    CUtensorMap tk, tv;
+    if (!encode_pages(&tk, k_pages, rows, d, box_rows) ||
+        !encode_pages(&tv, v_pages, rows, d, box_rows))
+        return TREE_ATTN_ERR_CUDA;
+
+    VerifyArgs a;
+    a.q = q;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.tree_k = tree_k;
+    a.tree_v = tree_v;
+    a.mask = mask;
+    a.out = out;
+    a.lse = lse;
+    a.ws = static_cast<float*>(workspace);
+    a.status = status;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.T = T;
+    a.P = page_size;
+    a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    a.n_ctas = n_ctas;
+    a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+    const cudaError_t e = launch_verify(a, &tk, &tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_attn_verify(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                     const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                     const uint16_t* tree_k, const uint16_t* tree_v, const uint64_t* mask,
+                     uint16_t* out, float* lse, int B, int Hq, int Hkv, int d, int T,
+                     int page_size, int num_pages, float softmax_scale, void* workspace,
+                     size_t workspace_bytes, int32_t* status, void* stream) {
+    return tree_attn_verify_ctas(q, k_pages, v_pages, block_table, max_pages_per_seq, seq_lens,
+                                 tree_k, tree_v, mask, out, lse, B, Hq, Hkv, d, T, page_size,
+                                 num_pages, softmax_scale, workspace, workspace_bytes, status,
+                                 stream, 0);
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// CPU check of the prefix-pass work partition in csrc/layout.h:
+//   * the segments of all CTAs cover every (unit, chunk) exactly once,
+//   * partial-result slots (unit + cta) are unique and < units + CTAs,
+//   * the merge side's slot range for a unit (cta_of of the unit's first and
+//     last work-line positions) names exactly the CTAs that wrote it,
+//   * the descriptor helpers put each field where the bit layout says.
+// Prints "OK" and exits 0, or prints the first failure and exits 1.
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <set>
+#include <utility>
+#include <vector>
+
+#include "layout.h"
+
+using namespace treeattn;
+
+static unsigned long long rng_state = 12345;
+static unsigned next_rand() {
+    rng_state = rng_state * 6364136223846793005ULL + 1442695040888963407ULL;
+    return static_cast<unsigned>(rng_state >> 33);
+}
+
+#define CHECK(cond, ...)                                     \
+    do {                                                     \
+        if (!(cond)) {                                       \
+            std::printf("FAIL %s:%d: ", __FILE__, __LINE__); \
+            std::printf(__VA_ARGS__);                        \
+            std::printf("\n");                               \
+            return false;                                    \
+        }                                                    \
+    } while (0)
+
+static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C,
+                            const std::vector<int32_t>& sl) {
+    const int upb = Hkv * RB;
+    std::map<std::pair<int, int>, int> covered;  // (unit, chunk) -> count
+    std::map<int, std::set<int>> writers;        // unit -> CTAs
+    std::set<long long> slots;
+    long long W = 0;
+    for (int c = 0; c < C; ++c) {
+        int b0;
+        long long base0, x0, x1;
+        plan_serial(sl.data(), B, P, maxp, upb, C, c, W, b0, base0, x0, x1);
+        Walker w;
+        w.init(sl.data(), B, P, maxp, upb, RB, b0, base0, x0, x1);
+        Segment s;
+        long long done = 0;
+        while (w.next(s)) {
+            CHECK(s.chunk_end > s.chunk_begin, "empty segment");
+            CHECK(s.unit == (s.b * Hkv + s.hk) * RB + s.rb, "unit index");
+            bool bad;
+            const int nch = chunks_of(clamp_seq_len(sl[s.b], P, maxp, bad));
+            CHECK(s.chunk_end <= nch, "segment past the sequence");
+            for (int ch = s.chunk_begin; ch < s.chunk_end; ++ch)
+                covered[std::make_pair(s.unit, ch)]++;
+            CHECK(slots.insert(static_cast<long long>(s.unit) + c).second, "slot reused");
+            CHECK(s.unit + c < B * upb + C, "slot out of range");
+            writers[s.unit].insert(c);
+            done += s.chunk_end - s.chunk_begin;
+        }
+        CHECK(done == x1 - x0, "CTA range not fully walked");
+    }
+    long long base = 0;
+    for (int b = 0; b < B; ++b) {
+        bool bad;
+        const int nch = chunks_of(clamp_seq_len(sl[b], P, maxp, bad));
+        for (int urel = 0; urel < upb; ++urel) {
+            const int unit = b * upb + urel;
+            for (int ch = 0; ch < nch; ++ch) {
+                const int n = covered[std::make_pair(unit, ch)];
+                CHECK(n == 1, "unit %d chunk %d covered %d times", unit, ch, n);
+            }
+            std::set<int> want;
+            if (nch > 0) {
+                const long long us = base + static_cast<long long>(urel) * nch;
+                const int cf = cta_of(us, W, C), cl = cta_of(us + nch - 1, W, C);
+                for (int c = cf; c <= cl; ++c)
+                    if (cta_has_work(c, W, C)) want.insert(c);
+            }
+            CHECK(want == writers[unit], "merge-side CTA range mismatch for unit %d", unit);
+        }
+        base += static_cast<long long>(upb) * nch;
+    }
+    CHECK(base == W, "work-line length");
+    return true;
+}
+
+static bool check_descriptors() {
+    const uint64_t d = smem_desc_sw128(0x12340, 8192, 1024);
+    CHECK((d & 0x3FFF) == (0x12340 >> 4), "start address field");
+    CHECK(((d >> 16) & 0x3FFF) == 8192 / 16, "LBO field");
+    CHECK(((d >> 32) & 0x3FFF) == 1024 / 16, "SBO field");
+    CHECK(((d >> 46) & 0x3) == 1, "version field");
+    CHECK(((d >> 49) & 0x7) == 0, "base offset field");
+    CHECK(((d >> 61) & 0x7) == 2, "swizzle field");
+    const uint32_t i = idesc_bf16_f32(128, 64, false, true);
+    CHECK(((i >> 4) & 3) == 1 && ((i >> 7) & 7) == 1 && ((i >> 10) & 7) == 1, "formats");
+    CHECK(((i >> 15) & 1) == 0 && ((i >> 16) & 1) == 1, "major bits");
+    CHECK(((i >> 17) & 0x3F) == 64 / 8 && ((i >> 24) & 0x1F) == 128 / 16, "shape fields");
+    // 128-byte swizzle: chunk c of row r lands at chunk c ^ (r % 8) of that row
+    for (uint32_t r = 0; r < 16; ++r)
+        for (uint32_t c = 0; c < 8; ++c) {
+            const uint32_t off = sw128_offset(r, c);
+            CHECK(off / 128 == r, "row of swizzled chunk");
+            CHECK(((off % 128) / 16) == (c ^ (r % 8)), "swizzled chunk position");
+        }
+    return true;
+}
+
+int main() {
+    if (!check_descriptors()) return 1;
+    const int Ps[4] = {16, 32, 64, 128};
+    for (int trial = 0; trial < 400; ++trial) {
+        const int B = 1 + next_rand() % 9;
+        const int Hkv = 1 + next_rand() % 4;
+        const int RB = 1 + next_rand() % 2;
+        const int P = Ps[next_rand() % 4];
+        const int maxp = 1 + next_rand() % 12;
+        const int C = 1 + next_rand() % 40;
+        std::vector<int32_t> sl(B);
+        for (int b = 0; b < B; ++b) {
+            const unsigned kind = next_rand() % 6;
+            if (kind == 0)
+                sl[b] = 0;
+            else if (kind == 1)
+                sl[b] = maxp * P;  // full
+            else if (kind == 2)
+                sl[b] = maxp * P + 5;  // too long: clamped
+            else
+                sl[b] = next_rand() % (maxp * P + 1);
+        }
+        if (!check_partition(B, Hkv, RB, P, maxp, C, sl)) {
+            std::printf("  at trial %d (B=%d Hkv=%d RB=%d P=%d maxp=%d C=%d)\n", trial, B, Hkv,
+                        RB, P, maxp, C);
+            return 1;
+        }
+    }
+    std::printf("OK\n");
+    return 0;
+}

@@ -1,0 +1,121 @@
+"""The C ABI library: loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (CPU only)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import speculative_decoding_tree_split_gb300 as ta
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ta.build()
+    return ta.load()
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(HEADER_DIR)):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            names += re.findall(r"TREE_ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tree_mask_build", "tree_attn_workspace_size", "tree_attn_verify"):
+        assert n in names
+    assert set(names) == set(ta.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert ta.version() == 10000
+
+
+def test_only_declared_symbols_are_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ta.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(declared_functions())
+
+
+# Fake, never-dereferenced device addresses: the host checks below return
+# before any CUDA call.
+A16 = 0x10000
+
+
+def _verify(lib, **kw):
+    args = dict(q=A16, k=A16, v=A16, bt=A16, maxp=4, sl=A16, tk=A16, tv=A16, mask=A16, out=A16,
+                lse=A16, B=2, Hq=8, Hkv=2, d=128, T=4, P=64, num_pages=8, scale=0.1, ws=A16,
+                ws_bytes=1 << 30, status=None, stream=None)
+    args.update(kw)
+    return lib.tree_attn_verify_ctas(
+        args["q"], args["k"], args["v"], args["bt"], args["maxp"], args["sl"], args["tk"],
+        args["tv"], args["mask"], args["out"], args["lse"], args["B"], args["Hq"], args["Hkv"],
+        args["d"], args["T"], args["P"], args["num_pages"], args["scale"], args["ws"],
+        args["ws_bytes"], args["status"], args["stream"], 8)
+
+
+@pytest.mark.parametrize("kw", [dict(T=0), dict(T=65), dict(Hq=6, Hkv=4), dict(d=96),
+                                dict(P=48), dict(maxp=0), dict(num_pages=0),
+                                dict(num_pages=1 << 24, Hkv=8, P=64), dict(scale=float("nan"))])
+def test_verify_rejects_bad_shapes(lib, kw):
+    assert _verify(lib, **kw) == -2
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "bt", "sl", "tk", "tv", "mask", "out", "lse"])
+def test_verify_rejects_null(lib, name):
+    assert _verify(lib, **{name: None}) == -1
+
+
+@pytest.mark.parametrize("name,addr", [("q", A16 + 8), ("k", A16 + 2), ("out", A16 + 4),
+                                       ("mask", A16 + 4), ("lse", A16 + 2), ("bt", A16 + 1),
+                                       ("status", A16 + 2)])
+def test_verify_rejects_misaligned(lib, name, addr):
+    assert _verify(lib, **{name: addr}) == -3
+
+
+def test_verify_rejects_small_workspace(lib):
+    need = lib.tree_attn_workspace_size_ctas(2, 8, 2, 128, 4, 64, 8)
+    assert need > 0
+    assert _verify(lib, ws_bytes=need - 1) == -4
+    assert _verify(lib, ws=None) == -4
+    assert _verify(lib, ws=A16 + 16) == -4
+
+
+def test_empty_batch_enqueues_nothing(lib):
+    assert _verify(lib, B=0, q=None) == 0
+
+
+def test_workspace_size_formula(lib):
+    # slots = units + CTAs; slot = (2*128 + 128*d) floats; rounded to 256 B
+    for (B, Hq, Hkv, d, T, C) in [(1, 32, 8, 128, 12, 152), (64, 32, 8, 128, 4, 152),
+                                  (2, 4, 1, 64, 4, 7), (1, 8, 1, 128, 64, 10)]:
+        G = Hq // Hkv
+        RB = (T * G + 127) // 128
+        slots = B * Hkv * RB + C
+        want = slots * (2 * 128 + 128 * d) * 4
+        want = (want + 255) // 256 * 256
+        assert lib.tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, 64, C) == want
+    assert lib.tree_attn_workspace_size_ctas(1, 8, 3, 128, 4, 64, 8) == 0
+
+
+def test_mask_build_host_checks(lib):
+    assert lib.tree_mask_build(None, 4, A16, None, None) == -1
+    assert lib.tree_mask_build(A16, 0, A16, None, None) == -2
+    assert lib.tree_mask_build(A16, 65, A16, None, None) == -2
+    assert lib.tree_mask_build(A16, 4, A16 + 4, None, None) == -3
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        ta.mask_build(torch.tensor([-1, 0], dtype=torch.int32))
