@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark of split tree attention (verification attention of tree
+speculative decoding) on one or more GPUs of one node.
+
+A step is one pass of the whole hot path over one batch: tree_mask_build
+(ancestor bitmasks of the draft tree) followed by tree_attn_verify (prefix
+pass split over the paged KV cache, tree-masked suffix pass, log-sum-exp
+merge), through the C ABI.
+
+    python bench.py [--config llama8b] [--steps K] [--warmup W]
+    python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
+    python bench.py --impl reference     # the fp64 CPU oracle, timed alone
+
+Prints one JSON line (rank 0).  ``value`` is verified tree tokens per second
+over all ranks (B*T tokens per step and rank; each rank runs an independent
+replica, so scaling is weak).  Inputs stay resident in HBM during the timed
+region; the KV cache is replicated R times on the device and the steps rotate
+through the replicas so that every step reads K/V that is not in L2
+(R * KV bytes >= 4 x L2).  The timed steps are replayed from one CUDA graph.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+from workloads import CONFIGS, make_workload  # noqa: E402
+
+METRIC = "verified tree tokens/s per layer"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the prefix-pass
+# kernel from an ncu capture, keyed by workload, valid only for the kernel
+# source whose SHA-256 is recorded with it (see profiles/).
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", choices=sorted(CONFIGS), default="llama8b")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="bound on the CPU-baseline sample (oracle wall time)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    with open(os.path.join(_ROOT, "speculative_decoding_tree_split_gb300", "csrc",
+                           "kernels.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def workload_desc(cfg):
+    return cfg.describe()
+
+
+def algorithmic_bytes(wl):
+    """Bytes one verify call must move (prefix K/V dominates)."""
+    c = wl.cfg
+    kv = wl.kv_bytes()
+    q = c.B * c.T * c.Hq * c.d * 2
+    tree = c.B * c.T * c.Hkv * c.d * 2 * 2
+    out = c.B * c.T * c.Hq * c.d * 2
+    lse = c.B * c.T * c.Hq * 4
+    tables = wl.block_table.numel() * 4 + c.B * 4 + c.T * 8 + c.T * 4
+    return {"kv": kv, "prefix_kernel": kv + q, "call": kv + q + tree + out + lse + tables}
+
+
+class ClockSampler:
+    """nvidia-smi clocks sampled every 200 ms while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def smi_gpu_id(props, local):
+    """An nvidia-smi -i selector for this process's GPU."""
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    if local < len(ids):
+        return ids[local].strip()
+    return str(local)
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the fp64 oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_tokens_per_s(wl, budget_s, max_tokens=None):
+    """Time the oracle on whole tree tokens (all Hq heads of one (b, i)),
+    round-robin over the batch, until `budget_s` of wall time is spent."""
+    import oracle
+    orc = oracle.get()
+    c = wl.cfg
+    mask = orc.tree_mask(wl.parents.tolist())
+    threads = len(os.sched_getaffinity(0))
+    tokens = [(b, i) for b in range(c.B) for i in range(c.T)]
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        b, i = tokens[done % len(tokens)]
+        rows = np.array([(b, i, h) for h in range(c.Hq)], dtype=np.int32)
+        orc.verify_rows(wl, mask, rows, threads=threads)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_tokens is not None and done >= max_tokens):
+            break
+    return done / el, done, el, threads
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    wl = make_workload(cfg)
+    import oracle
+    orc = oracle.get()
+    mask = orc.tree_mask(wl.parents.tolist())
+    threads = len(os.sched_getaffinity(0))
+    tokens = [(b, i) for b in range(cfg.B) for i in range(cfg.T)]
+
+    def step(n):
+        b, i = tokens[n % len(tokens)]
+        rows = np.array([(b, i, h) for h in range(cfg.Hq)], dtype=np.int32)
+        orc.verify_rows(wl, mask, rows, threads=threads)
+
+    for n in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for n in range(args.steps):
+        step(args.warmup + n)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    emit({"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": workload_desc(cfg)},
+          "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                           "sample": f"each step = one tree token (all {cfg.Hq} query heads of "
+                                     f"one (sequence, node)) of the workload, round-robin"},
+          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import speculative_decoding_tree_split_gb300 as ta
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta.build()
+    ta.load()
+
+    cfg = CONFIGS[args.config]
+    wl = make_workload(cfg, seed=cfg.seed + rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 132 * 1024 * 1024
+    kv_alloc = wl.k_pages.numel() * 2 * 2
+    R = max(2, math.ceil(4 * l2 / max(kv_alloc, 1)))
+
+    # resident inputs
+    parents = wl.parents.to(dev)
+    q = wl.q.to(dev)
+    bt = wl.block_table.to(dev)
+    sl = wl.seq_lens.to(dev)
+    tk = wl.tree_k.to(dev)
+    tv = wl.tree_v.to(dev)
+    kps = [wl.k_pages.to(dev) for _ in range(R)]
+    vps = [wl.v_pages.to(dev) for _ in range(R)]
+    mask = torch.empty(cfg.T, dtype=torch.int64, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(cfg.B, cfg.T, cfg.Hq, dtype=torch.float32, device=dev)
+    ws_bytes = ta.workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.T, 0, cfg.page)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(r):
+        ta.mask_build(parents, mask_out=mask, status=status)
+        ta.verify(q, kps[r % R], vps[r % R], bt, sl, tk, tv, mask, out=out, lse=lse,
+                  workspace=ws, status=status, softmax_scale=wl.scale)
+
+    def prefix_only(r):
+        ta.prefix_pass(q, kps[r % R], vps[r % R], bt, sl, ws, status=status,
+                       softmax_scale=wl.scale)
+
+    # eager warm-up (also sets the kernels' shared-memory opt-in before capture)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for r in range(max(args.warmup, 1)):
+            step(r)
+            prefix_only(r)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for r in range(n):
+                fn(r)
+        return g
+
+    K, W = args.steps, args.warmup
+    g_timed = capture(step, K)
+    g_warm = capture(step, max(W, 1))
+    g_prefix = capture(prefix_only, K)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed(graph):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier()
+        s.record()
+        graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        barrier()
+        return s.elapsed_time(e)
+
+    # warm-up replays (W steps), then keep the GPU loaded ~1 s so the clock
+    # sampler sees the timed region's clocks, then the timed K steps.
+    g_warm.replay()
+    sampler = ClockSampler(smi_gpu_id(props, local))
+    if not args.no_clocks:
+        sampler.start()
+    t_end = time.perf_counter() + 1.2
+    while time.perf_counter() < t_end:
+        g_warm.replay()
+        torch.cuda.synchronize()
+    ms_total = timed(g_timed)
+    ms_prefix_total = timed(g_prefix)
+    clocks = sampler.stop() if not args.no_clocks else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+
+    ms_step = ms_total / K
+    ms_prefix = ms_prefix_total / K
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step, ms_prefix], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_prefix = float(t[0]), float(t[1])
+    tokens_per_step = cfg.B * cfg.T * world
+    value = tokens_per_step / (ms_step * 1e-3)
+
+    nbytes = algorithmic_bytes(wl)
+    peak, peak_src = measured_hbm_peak()
+    achieved = nbytes["prefix_kernel"] / (ms_prefix * 1e-3) / 1e9
+    sha = kernel_source_sha()
+    traffic = None
+    rec = NCU_TRAFFIC.get(args.config)
+    if rec is not None and rec[0] == sha:
+        traffic = rec[1]
+
+    # end to end through the public API: pinned host inputs -> device, the
+    # step, out/lse -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        h = {k: v.pin_memory() for k, v in dict(
+            parents=wl.parents, q=wl.q, k=wl.k_pages, v=wl.v_pages, bt=wl.block_table,
+            sl=wl.seq_lens, tk=wl.tree_k, tv=wl.tree_v).items()}
+        d = dict(parents=parents, q=q, k=kps[0], v=vps[0], bt=bt, sl=sl, tk=tk, tv=tv)
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+        n_e2e = max(3, min(K, int(20e9 // max(h2d, 1))))
+
+        def e2e_step():
+            for key in h:
+                d[key].copy_(h[key], non_blocking=True)
+            ta.mask_build(d["parents"], mask_out=mask, status=status)
+            ta.verify(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["tk"], d["tv"], mask, out=out,
+                      lse=lse, workspace=ws, status=status, softmax_scale=wl.scale)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        e.record()
+        torch.cuda.synchronize()
+        ms_e2e = s.elapsed_time(e) / n_e2e
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t[0])
+        e2e = {"value": tokens_per_step / (ms_e2e * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": ms_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n_tok, el, threads = oracle_tokens_per_s(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n_tok} tree tokens (all {cfg.Hq} query heads each) of this "
+                         f"workload, round-robin, {el:.1f} s of fp64 oracle time"}
+
+    if rank == 0:
+        emit({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "tokens_per_step_per_gpu": cfg.B * cfg.T,
+                       "l2": f"{R} rotating device copies of the KV cache "
+                             f"({R * kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)",
+                       "parallelism": f"replicas x{world}", "timing": "one CUDA graph of the "
+                       "K steps, CUDA events on the replay stream"},
+            "us_per_call": ms_step * 1e3,
+            "call_hbm_gbs": nbytes["call"] / (ms_step * 1e-3) / 1e9,
+            "prefix_kernel_us": ms_prefix * 1e3,
+            "roofline": {"bound": "hbm", "kernel": "prefix_pass_kernel",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": nbytes["prefix_kernel"],
+                         "peak_source": peak_src, "kernel_sha": sha},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * K,
+            "cpu_baseline": cpu,
+        })
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -162,6 +162,38 @@ TREE_ATTN_API int tree_attn_verify_ctas(const uint16_t *q, const uint16_t *k_pag
 TREE_ATTN_API size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T,
                                                    int page_size, int n_ctas);
 
+/*
+ * tree_attn_prefix_pass / tree_attn_suffix_merge -- the two passes of
+ * tree_attn_verify as separate calls (tree_attn_verify_ctas == prefix pass
+ * then suffix merge, same arguments).  The prefix pass ("attention from query
+ * to the prefix context ... no custom mask needed", pith.science review,
+ * "What carries the argument") writes one partial result (running max m,
+ * sum l, unnormalised accumulator acc, base-2 exponent domain) per split of
+ * the prefix into `workspace`.  The suffix merge computes the tree part under
+ * `mask` and merges it with every partial (merge_attentions over disjoint KV
+ * chunks, verdict record supporting_citations) into out / lse.
+ *
+ * Both calls must see the same B, Hq, Hkv, d, T, page_size,
+ * max_pages_per_seq, seq_lens contents, softmax_scale, n_ctas (<= 0: one per
+ * SM) and workspace, in stream order.  Arguments, layouts, alignment and
+ * return codes as for tree_attn_verify; the merge reads no K/V pages.
+ */
+TREE_ATTN_API int tree_attn_prefix_pass(const uint16_t *q, const uint16_t *k_pages,
+                                        const uint16_t *v_pages, const int32_t *block_table,
+                                        int max_pages_per_seq, const int32_t *seq_lens, int B,
+                                        int Hq, int Hkv, int d, int T, int page_size,
+                                        int num_pages, float softmax_scale, void *workspace,
+                                        size_t workspace_bytes, int n_ctas, int32_t *status,
+                                        void *stream);
+
+TREE_ATTN_API int tree_attn_suffix_merge(const uint16_t *q, const int32_t *seq_lens,
+                                         int max_pages_per_seq, const uint16_t *tree_k,
+                                         const uint16_t *tree_v, const uint64_t *mask,
+                                         uint16_t *out, float *lse, int B, int Hq, int Hkv, int d,
+                                         int T, int page_size, float softmax_scale,
+                                         const void *workspace, size_t workspace_bytes,
+                                         int n_ctas, void *stream);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 TREE_ATTN_API int tree_attn_version(void);
 

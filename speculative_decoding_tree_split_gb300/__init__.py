@@ -21,6 +21,8 @@ from ._lib import (  # noqa: F401
     TreeAttnError,
     load,
     mask_build,
+    prefix_pass,
+    suffix_merge,
     verify,
     version,
     workspace_size,

@@ -39,6 +39,8 @@ EXPORTED = (
     "tree_attn_verify_ctas",
     "tree_attn_workspace_size_ctas",
     "tree_attn_version",
+    "tree_attn_prefix_pass",
+    "tree_attn_suffix_merge",
 )
 
 
@@ -75,6 +77,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_verify.restype = i32
     lib.tree_attn_verify_ctas.argtypes = verify_args + [i32]
     lib.tree_attn_verify_ctas.restype = i32
+    lib.tree_attn_prefix_pass.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
+                                          i32, f32, vp, sz, i32, vp, vp]
+    lib.tree_attn_prefix_pass.restype = i32
+    lib.tree_attn_suffix_merge.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                           i32, i32, f32, vp, sz, i32, vp]
+    lib.tree_attn_suffix_merge.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -189,6 +197,53 @@ def verify(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
     if rc != 0:
         raise TreeAttnError("tree_attn_verify", rc)
     return out, lse
+
+
+def prefix_pass(q, k_pages, v_pages, block_table, seq_lens, workspace, *, T=None,
+                status=None, softmax_scale=None, stream=None, n_ctas: int = 0) -> None:
+    """Prefix pass alone: partial results of every split into `workspace`."""
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 4)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(workspace, "workspace", (torch.uint8,))
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    rc = load().tree_attn_prefix_pass(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), B, Hq, Hkv, d, T, P, num_pages, float(softmax_scale), _ptr(workspace),
+        workspace.numel(), int(n_ctas), _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_prefix_pass", rc)
+
+
+def suffix_merge(q, seq_lens, max_pages_per_seq: int, page_size: int, tree_k, tree_v, mask,
+                 workspace, out, lse, *, softmax_scale=None, stream=None,
+                 n_ctas: int = 0) -> None:
+    """Tree-masked suffix pass and log-sum-exp merge of the prefix partials."""
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 4)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(tree_k, "tree_k", bf, 4)
+    _check(tree_v, "tree_v", bf, 4)
+    _check(mask, "mask", _BITS64, 1)
+    _check(out, "out", bf, 4)
+    _check(lse, "lse", (torch.float32,), 3)
+    _check(workspace, "workspace", (torch.uint8,))
+    B, T, Hq, d = q.shape
+    Hkv = tree_k.shape[2]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    rc = load().tree_attn_suffix_merge(
+        _ptr(q), _ptr(seq_lens), int(max_pages_per_seq), _ptr(tree_k), _ptr(tree_v), _ptr(mask),
+        _ptr(out), _ptr(lse), B, Hq, Hkv, d, T, int(page_size), float(softmax_scale),
+        _ptr(workspace), workspace.numel(), int(n_ctas), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_suffix_merge", rc)
 
 
 def version() -> int:

@@ -641,6 +641,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     // ---------------- teardown
+    __syncwarp();  // lanes 1-31 of the producer / MMA warps wait for lane 0
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 5) {
@@ -828,7 +829,7 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 }
 
 template <int D>
-cudaError_t launch_verify_d(const VerifyArgs& v, const void* tmap_k, const void* tmap_v,
+cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void* tmap_v,
                             cudaStream_t stream) {
     using S = PrefixShape<D>;
     static int configured_for = -1;  // device on which the smem opt-in was applied
@@ -843,7 +844,6 @@ cudaError_t launch_verify_d(const VerifyArgs& v, const void* tmap_k, const void*
     }
     const int G = v.Hq / v.Hkv;
     const int M = v.T * G;
-    const int RB = (M + kRows - 1) / kRows;
     PrefixArgs pa;
     pa.block_table = v.block_table;
     pa.seq_lens = v.seq_lens;
@@ -856,7 +856,7 @@ cudaError_t launch_verify_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.G = G;
     pa.T = v.T;
     pa.M = M;
-    pa.RB = RB;
+    pa.RB = (M + kRows - 1) / kRows;
     pa.P = v.P;
     pa.max_pages = v.max_pages;
     pa.num_pages = v.num_pages;
@@ -864,10 +864,15 @@ cudaError_t launch_verify_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.scale_log2 = v.scale_log2;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
-    e = launch_pdl(prefix_pass_kernel<D>, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv,
-                   pa);
-    if (e != cudaSuccess) return e;
+    return launch_pdl(prefix_pass_kernel<D>, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk,
+                      tv, pa);
+}
 
+template <int D>
+cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
+    const int G = v.Hq / v.Hkv;
+    const int M = v.T * G;
+    const int RB = (M + kRows - 1) / kRows;
     MergeArgs ma;
     ma.q = v.q;
     ma.tree_k = v.tree_k;
@@ -900,10 +905,15 @@ cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int
     return launch_pdl(tree_mask_kernel, dim3(1), dim3(32), 0, stream, parents, T, mask, status);
 }
 
-cudaError_t launch_verify(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
                           cudaStream_t stream) {
-    if (a.d == 128) return launch_verify_d<128>(a, tmap_k, tmap_v, stream);
-    return launch_verify_d<64>(a, tmap_k, tmap_v, stream);
+    if (a.d == 128) return launch_prefix_d<128>(a, tmap_k, tmap_v, stream);
+    return launch_prefix_d<64>(a, tmap_k, tmap_v, stream);
+}
+
+cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream) {
+    if (a.d == 128) return launch_merge_d<128>(a, stream);
+    return launch_merge_d<64>(a, stream);
 }
 
 }  // namespace treeattn

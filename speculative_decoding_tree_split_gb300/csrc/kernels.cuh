@@ -30,9 +30,12 @@ struct VerifyArgs {
 cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int32_t* status,
                               cudaStream_t stream);
 
-// Enqueue the prefix pass and the suffix + merge pass.  `tmap_k`/`tmap_v`
-// point at encoded CUtensorMap objects (host memory, copied into the launch).
-cudaError_t launch_verify(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+// Enqueue the prefix pass (partials into a.ws).  `tmap_k`/`tmap_v` point at
+// encoded CUtensorMap objects (host memory, copied into the launch).
+cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
                           cudaStream_t stream);
+
+// Enqueue the suffix pass + merge (reads the partials in a.ws).
+cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream);
 
 }  // namespace treeattn

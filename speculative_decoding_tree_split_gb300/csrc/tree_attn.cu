@@ -75,6 +75,32 @@ bool encode_pages(CUtensorMap* map, const void* base, long long rows, int d, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Checks shared by the verify, prefix-pass and merge entry points.
+int check_common(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pages_per_seq,
+                 float softmax_scale) {
+    if (!shape_ok(B, Hq, Hkv, d, T, page_size) || max_pages_per_seq < 1 ||
+        !std::isfinite(softmax_scale))
+        return TREE_ATTN_ERR_SHAPE;
+    return TREE_ATTN_OK;
+}
+
+int resolve_ctas(int n_ctas) { return n_ctas > 0 ? n_ctas : sm_count(); }
+
+float to_log2(float softmax_scale) {
+    return static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+}
+
+int prefix_impl(VerifyArgs& a, const uint16_t* k_pages, const uint16_t* v_pages,
+                cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.num_pages) * a.Hkv * a.P;
+    const int box_rows = a.P < kChunk ? a.P : kChunk;
+    CUtensorMap tk, tv;
+    if (!encode_pages(&tk, k_pages, rows, a.d, box_rows) ||
+        !encode_pages(&tv, v_pages, rows, a.d, box_rows))
+        return TREE_ATTN_ERR_CUDA;
+    return launch_prefix(a, &tk, &tv, stream) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -106,6 +132,85 @@ size_t tree_attn_workspace_size(int B, int Hq, int Hkv, int d, int T, int max_se
     return tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, page_size, 0);
 }
 
+int tree_attn_prefix_pass(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                          const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, int B, int Hq, int Hkv, int d, int T,
+                          int page_size, int num_pages, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, int n_ctas, int32_t* status, void* stream) {
+    int rc = check_common(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, softmax_scale);
+    if (rc != TREE_ATTN_OK) return rc;
+    if (num_pages < 1 || static_cast<long long>(num_pages) * Hkv * page_size >= (1LL << 31))
+        return TREE_ATTN_ERR_SHAPE;
+    if (B == 0) return TREE_ATTN_OK;
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens) return TREE_ATTN_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    n_ctas = resolve_ctas(n_ctas);
+    if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
+        return TREE_ATTN_ERR_WORKSPACE;
+    VerifyArgs a = {};
+    a.q = q;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.ws = static_cast<float*>(workspace);
+    a.status = status;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.T = T;
+    a.P = page_size;
+    a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    a.n_ctas = n_ctas;
+    a.scale_log2 = to_log2(softmax_scale);
+    return prefix_impl(a, k_pages, v_pages, static_cast<cudaStream_t>(stream));
+}
+
+int tree_attn_suffix_merge(const uint16_t* q, const int32_t* seq_lens, int max_pages_per_seq,
+                           const uint16_t* tree_k, const uint16_t* tree_v, const uint64_t* mask,
+                           uint16_t* out, float* lse, int B, int Hq, int Hkv, int d, int T,
+                           int page_size, float softmax_scale, const void* workspace,
+                           size_t workspace_bytes, int n_ctas, void* stream) {
+    int rc = check_common(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, softmax_scale);
+    if (rc != TREE_ATTN_OK) return rc;
+    if (B == 0) return TREE_ATTN_OK;
+    if (!q || !seq_lens || !tree_k || !tree_v || !mask || !out || !lse) return TREE_ATTN_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(tree_k, 16) || !aligned(tree_v, 16) || !aligned(out, 16) ||
+        !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8))
+        return TREE_ATTN_ERR_ALIGN;
+    n_ctas = resolve_ctas(n_ctas);
+    if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
+        return TREE_ATTN_ERR_WORKSPACE;
+    VerifyArgs a = {};
+    a.q = q;
+    a.seq_lens = seq_lens;
+    a.tree_k = tree_k;
+    a.tree_v = tree_v;
+    a.mask = mask;
+    a.out = out;
+    a.lse = lse;
+    a.ws = static_cast<float*>(const_cast<void*>(workspace));
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.T = T;
+    a.P = page_size;
+    a.max_pages = max_pages_per_seq;
+    a.n_ctas = n_ctas;
+    a.scale_log2 = to_log2(softmax_scale);
+    return launch_merge(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TREE_ATTN_OK
+                                                                           : TREE_ATTN_ERR_CUDA;
+}
+
 int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
                           const int32_t* block_table, int max_pages_per_seq,
                           const int32_t* seq_lens, const uint16_t* tree_k,
@@ -113,10 +218,9 @@ int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint
                           float* lse, int B, int Hq, int Hkv, int d, int T, int page_size,
                           int num_pages, float softmax_scale, void* workspace,
                           size_t workspace_bytes, int32_t* status, void* stream, int n_ctas) {
-    if (!shape_ok(B, Hq, Hkv, d, T, page_size) || max_pages_per_seq < 1 || num_pages < 1 ||
-        !std::isfinite(softmax_scale))
-        return TREE_ATTN_ERR_SHAPE;
-    if (static_cast<long long>(num_pages) * Hkv * page_size >= (1LL << 31))
+    int rc = check_common(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, softmax_scale);
+    if (rc != TREE_ATTN_OK) return rc;
+    if (num_pages < 1 || static_cast<long long>(num_pages) * Hkv * page_size >= (1LL << 31))
         return TREE_ATTN_ERR_SHAPE;
     if (B == 0) return TREE_ATTN_OK;
     if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !tree_k || !tree_v || !mask ||
@@ -126,20 +230,13 @@ int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint
         !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8) || !aligned(status, 4))
         return TREE_ATTN_ERR_ALIGN;
-    if (n_ctas <= 0) n_ctas = sm_count();
+    n_ctas = resolve_ctas(n_ctas);
     if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
         return TREE_ATTN_ERR_WORKSPACE;
 
-    const long long rows = static_cast<long long>(num_pages) * Hkv * page_size;
-    const int box_rows = page_size < kChunk ? page_size : kChunk;
-    CUtensorMap tk, tv;
-    if (!encode_pages(&tk, k_pages, rows, d, box_rows) ||
-        !encode_pages(&tv, v_pages, rows, d, box_rows))
-        return TREE_ATTN_ERR_CUDA;
-
-    VerifyArgs a;
+    VerifyArgs a = {};
     a.q = q;
     a.k_pages = k_pages;
     a.v_pages = v_pages;
@@ -161,9 +258,11 @@ int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint
     a.max_pages = max_pages_per_seq;
     a.num_pages = num_pages;
     a.n_ctas = n_ctas;
-    a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-    const cudaError_t e = launch_verify(a, &tk, &tv, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+    a.scale_log2 = to_log2(softmax_scale);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = prefix_impl(a, k_pages, v_pages, st);
+    if (rc != TREE_ATTN_OK) return rc;
+    return launch_merge(a, st) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 
 int tree_attn_verify(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
