@@ -194,6 +194,46 @@ TREE_ATTN_API int tree_attn_suffix_merge(const uint16_t *q, const int32_t *seq_l
                                          const void *workspace, size_t workspace_bytes,
                                          int n_ctas, void *stream);
 
+/*
+ * tree_attn_verify_noalloc -- tree_attn_verify for callers that cannot
+ * allocate device memory.  (The paper has no counterpart: this is a
+ * deployment convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc at the point where they run attention:
+ * code that runs inside a caller-managed memory pool with a fixed budget,
+ * plug-ins of a host engine that forbids allocations after start-up, or
+ * tools that must not grow the process's device footprint.  This entry point
+ * takes the same inputs and outputs as tree_attn_verify but no workspace: the
+ * per-split partial results go to a scratch array that is part of the
+ * library itself (TREE_ATTN_NOALLOC_SCRATCH_BYTES, 16 MiB, reserved on every
+ * GPU that loads the library until the process exits).
+ *
+ *   - Sizes whose partial results do not fit in the array are rejected with
+ *     TREE_ATTN_ERR_SCRATCH_LIMIT (nothing is enqueued).  The need is
+ *     (B*Hkv*ceil(T*Hq/Hkv/128) + SM count) * (256 + 128*d) * 4 bytes, e.g.
+ *     a batch of 1 with 8 KV heads and d = 128 on 152 SMs needs 10.6 MB.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.  No call allocates or frees memory.
+ *   - All calls share the one array and it keeps the previous call's
+ *     contents; nothing in it needs to start at zero.  Calls that overlap on
+ *     the GPU (e.g. on two streams at once) race on it and give wrong
+ *     results: serialise them.
+ * Arguments, layouts, alignment, status and other return codes as for
+ * tree_attn_verify.
+ */
+#define TREE_ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define TREE_ATTN_ERR_SCRATCH_LIMIT (-6) /* sizes exceed the built-in scratch array */
+
+TREE_ATTN_API int tree_attn_verify_noalloc(const uint16_t *q, const uint16_t *k_pages,
+                                           const uint16_t *v_pages, const int32_t *block_table,
+                                           int max_pages_per_seq, const int32_t *seq_lens,
+                                           const uint16_t *tree_k, const uint16_t *tree_v,
+                                           const uint64_t *mask, uint16_t *out, float *lse,
+                                           int B, int Hq, int Hkv, int d, int T, int page_size,
+                                           int num_pages, float softmax_scale, int32_t *status,
+                                           void *stream);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 TREE_ATTN_API int tree_attn_version(void);
 

@@ -25,6 +25,7 @@ ERRORS = {
     -3: "misaligned pointer",
     -4: "workspace missing, too small or misaligned",
     -5: "CUDA error",
+    -6: "sizes exceed the library's built-in scratch array",
 }
 STATUS_BAD_PARENT = 1
 STATUS_BAD_PAGE = 2
@@ -41,6 +42,7 @@ EXPORTED = (
     "tree_attn_version",
     "tree_attn_prefix_pass",
     "tree_attn_suffix_merge",
+    "tree_attn_verify_noalloc",
 )
 
 
@@ -83,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_suffix_merge.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                            i32, i32, f32, vp, sz, i32, vp]
     lib.tree_attn_suffix_merge.restype = i32
+    lib.tree_attn_verify_noalloc.argtypes = verify_args[:19] + [vp, vp]
+    lib.tree_attn_verify_noalloc.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
