@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(192, 1)
                misc->x1);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
             const bool ok = ptx::mbar_wait(b, parity);
-            const bool all = __all_sync(kFull, ok) && !*abort_flag;
+            const bool all = __all_sync(kFull, ok && !*abort_flag);
             if (!ok) fail();
             return all;
         };
@@ -688,6 +688,27 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// E consecutive fp32 accumulator values through L2 only, or zeros.
+template <int E>
+__device__ __forceinline__ void load_acc(const float* p, bool use, float* v) {
+    if (use) {
+        if constexpr (E == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(p));
+            v[0] = x.x;
+            v[1] = x.y;
+            v[2] = x.z;
+            v[3] = x.w;
+        } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
+            v[0] = x.x;
+            v[1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = 0.f;
+    }
+}
+
 constexpr int kMergeRows = 8;  // rows (warps) per CTA
 
 template <int D>
@@ -738,10 +759,8 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
         }
     }
 
-    // ---- partials of the prefix pass
-    ptx::grid_dep_wait();
-    ptx::grid_dep_launch();
-    if (!active) return;
+    // ---- where this unit's prefix partials live (inputs only, so this also
+    // runs before the prefix pass has finished)
     const int upb = a.Hkv * a.RB;
     long long W = 0, base_b = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -758,17 +777,42 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
     base_b *= upb;
     bool bad;
     const int nch = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
-    const size_t sf = static_cast<size_t>(slot_floats(D));
-    float mx = m_s;
     int c_first = 0, c_last = -1;
     if (nch > 0) {
         const long long ustart = base_b + static_cast<long long>(unit - b * upb) * nch;
         c_first = cta_of(ustart, W, a.n_ctas);
         c_last = cta_of(ustart + nch - 1, W, a.n_ctas);
-        for (int c = c_first + lane; c <= c_last; c += 32)
-            if (cta_has_work(c, W, a.n_ctas)) mx = fmaxf(mx, a.ws[(unit + c) * sf + r]);
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
     }
+
+    // ---- merge with the partials of the prefix pass
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+    if (!active) return;
+    const size_t sf = static_cast<size_t>(slot_floats(D));
+    const float* wsr = a.ws + r;  // row r of slot 0
+    const int nslots = c_last - c_first + 1;
+    // First round trip: (m, l) of up to 32 slots (lane j: slot c_first + j)
+    // and the accumulator rows of the first eight slots, all issued before
+    // any of them is used.  Partials are read through L2 only
+    // (ld.global.cg): the prefix grid wrote them while this grid was resident.
+    float m_j = kNegInf, l_j = 0.f;
+    if (lane < nslots && cta_has_work(c_first + lane, W, a.n_ctas)) {
+        const float* slot = wsr + (unit + c_first + lane) * sf;
+        m_j = __ldcg(slot);
+        l_j = __ldcg(slot + kRows);
+    }
+    float v[8][E];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const bool use = j < nslots && cta_has_work(c_first + j, W, a.n_ctas);
+        load_acc<E>(a.ws + (unit + c_first + j) * sf + 2 * kRows + static_cast<size_t>(r) * D +
+                        lane * E,
+                    use, v[j]);
+    }
+    float mx = fmaxf(m_s, m_j);
+    for (int c = c_first + 32 + lane; c <= c_last; c += 32)  // rare: > 32 slots
+        if (cta_has_work(c, W, a.n_ctas)) mx = fmaxf(mx, __ldcg(wsr + (unit + c) * sf));
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
     uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
     float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
     if (mx == kNegInf) {  // no key at all
@@ -778,26 +822,44 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
         return;
     }
     const float w_s = ptx::ex2(m_s - mx);
-    float total = l_s * w_s;
     float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = acc[e] * w_s;
-    for (int c = c_first; c <= c_last; ++c) {
-        if (!cta_has_work(c, W, a.n_ctas)) continue;
-        const float* slot = a.ws + (unit + c) * sf;
-        const float wc = ptx::ex2(slot[r] - mx);
-        total = fmaf(wc, slot[kRows + r], total);
-        const float* ac = slot + 2 * kRows + static_cast<size_t>(r) * D + lane * E;
-        if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(ac);
-            o[0] = fmaf(wc, v.x, o[0]);
-            o[1] = fmaf(wc, v.y, o[1]);
-            o[2] = fmaf(wc, v.z, o[2]);
-            o[3] = fmaf(wc, v.w, o[3]);
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(ac);
-            o[0] = fmaf(wc, v.x, o[0]);
-            o[1] = fmaf(wc, v.y, o[1]);
+    float wc = (m_j == kNegInf) ? 0.f : ptx::ex2(m_j - mx);
+    float total = l_s * w_s + warp_sum(wc * l_j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(kFull, wc, j);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
+    }
+    // Remaining slots, eight accumulator rows per round trip.
+    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
+        if (c0 != c_first) {
+            const int c = c0 + lane;
+            wc = 0.f;
+            float lc = 0.f;
+            if (c <= c_last && cta_has_work(c, W, a.n_ctas)) {
+                const float* slot = wsr + (unit + c) * sf;
+                wc = ptx::ex2(__ldcg(slot) - mx);
+                lc = __ldcg(slot + kRows);
+            }
+            total += warp_sum(wc * lc);
+        }
+        const int nb = min(32, c_last - c0 + 1);
+        for (int j0 = (c0 == c_first) ? 8 : 0; j0 < nb; j0 += 8) {
+            float wj[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                wj[j] = __shfl_sync(kFull, wc, j0 + j);
+                load_acc<E>(a.ws + (unit + c0 + j0 + j) * sf + 2 * kRows +
+                                static_cast<size_t>(r) * D + lane * E,
+                            j0 + j < nb && wj[j] != 0.f, v[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = fmaf(wj[j], v[j][e], o[e]);
         }
     }
     const float inv = 1.f / total;
