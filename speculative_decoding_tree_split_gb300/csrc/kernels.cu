@@ -108,20 +108,26 @@ __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict
 
 // ===========================================================================
 // Prefix pass
+//
+// Keys are processed in blocks of up to 128 (two 64-token steps of the work
+// line).  Every tcgen05.mma instruction costs about the same issue time
+// whatever its N, so S = Q.K^T uses N = 128 keys per instruction and P is
+// kept in TMEM as the A operand of O += P.V; per 128 keys the tensor pipe
+// sees 2*d/16 instructions.
 // ===========================================================================
+constexpr int kBlock = 2 * kChunk;  // keys per MMA block
+
 template <int D>
 struct PrefixShape {
-    static constexpr int DH = D / 64;                       // 128-byte d-halves
+    static constexpr int DH = D / 64;                       // 128-byte column blocks of d
     static constexpr int Q_BYTES = kRows * D * 2;           // Q tile, DH atom columns
-    static constexpr int QATOM_BYTES = kRows * 128;         // one atom column of Q / P
-    static constexpr int PBUF_BYTES = kRows * kChunk * 2;   // P (bf16) of one chunk
-    static constexpr int HALF_BYTES = kChunk * 128;         // 64 keys x 64 d of K or V
-    static constexpr int TILE_BYTES = DH * HALF_BYTES;      // K (or V) of one chunk
+    static constexpr int QATOM_BYTES = kRows * 128;         // one atom column of Q
+    static constexpr int HALF_BYTES = kBlock * 128;         // 128 keys x 64 d of K or V
+    static constexpr int TILE_BYTES = DH * HALF_BYTES;      // K (or V) of one block
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int NS = (D == 128) ? 4 : 8;           // ring depth
+    static constexpr int NS = (D == 128) ? 3 : 6;           // ring depth
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;
-    static constexpr int OFF_STAGE = OFF_P + 2 * PBUF_BYTES;
+    static constexpr int OFF_STAGE = OFF_Q + Q_BYTES;
     static constexpr int OFF_BAR = OFF_STAGE + NS * STAGE_BYTES;
     // barrier indices
     static constexpr int KV_FULL = 0;
@@ -131,16 +137,19 @@ struct PrefixShape {
     static constexpr int P_FULL = 2 * NS + 4;
     static constexpr int P_FREE = 2 * NS + 6;
     static constexpr int O_FULL = 2 * NS + 8;
-    static constexpr int O_FREE = 2 * NS + 10;
-    static constexpr int Q_FULL = 2 * NS + 12;
-    static constexpr int DRAIN = 2 * NS + 13;
-    static constexpr int NBAR = 2 * NS + 14;
+    static constexpr int O_FREE = 2 * NS + 9;
+    static constexpr int Q_FULL = 2 * NS + 10;
+    static constexpr int DRAIN = 2 * NS + 11;
+    static constexpr int NBAR = 2 * NS + 12;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
-    // TMEM columns: O[2] at [0, 2D), S[2] at [2D, 2D + 2*64).
+    // TMEM columns: O at [0, D); S[2] (fp32, 128 keys each) after it; P[2]
+    // (bf16 pairs, 64 columns each) after S.
     static constexpr int TM_O = 0;
-    static constexpr int TM_S = 2 * D;
-    static constexpr int TMEM_COLS = (2 * D + 2 * kChunk) > 256 ? 512 : 256;
+    static constexpr int TM_S = D;
+    static constexpr int TM_P = D + 2 * kBlock;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(TM_P + 2 * (kBlock / 2) <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
 };
@@ -234,7 +243,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D>
+// Blocks of one segment: block i covers work-line steps
+// [chunk_begin + 2i, min(chunk_begin + 2i + 2, chunk_end)).
+__device__ __forceinline__ int blocks_of(const Segment& sg) {
+    return (sg.chunk_end - sg.chunk_begin + 1) / 2;
+}
+
+template <int D, int F>
 __global__ void __launch_bounds__(192, 1)
     prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefixArgs a) {
@@ -261,9 +276,9 @@ __global__ void __launch_bounds__(192, 1)
             ptx::mbar_init(bar(S::S_FREE + i), 4);
             ptx::mbar_init(bar(S::P_FULL + i), 4);
             ptx::mbar_init(bar(S::P_FREE + i), 1);
-            ptx::mbar_init(bar(S::O_FULL + i), 1);
-            ptx::mbar_init(bar(S::O_FREE + i), 4);
         }
+        ptx::mbar_init(bar(S::O_FULL), 1);
+        ptx::mbar_init(bar(S::O_FREE), 4);
         ptx::mbar_init(bar(S::Q_FULL), 4);
         ptx::mbar_init(bar(S::DRAIN), 1);
         misc->abort = 0;
@@ -298,7 +313,7 @@ __global__ void __launch_bounds__(192, 1)
                    misc->x1);
             const uint64_t pol = ptx::policy_evict_first();
             const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
-            const int nsub = kChunk / Pb;                // boxes per chunk (pages < 64 tokens)
+            const int nsub = kChunk / Pb;                // boxes per 64-token step
             uint32_t jj = 0;
             bool ok = true;
             Segment sg;
@@ -307,7 +322,8 @@ __global__ void __launch_bounds__(192, 1)
                 const int L = clamp_seq_len(a.seq_lens[sg.b], a.P, a.max_pages, bad);
                 const int npages = (L + a.P - 1) / a.P;
                 const int32_t* bt = a.block_table + static_cast<size_t>(sg.b) * a.max_pages;
-                for (int ch = sg.chunk_begin; ch < sg.chunk_end; ++ch, ++jj) {
+                for (int ch = sg.chunk_begin; ch < sg.chunk_end; ch += 2, ++jj) {
+                    const int nh = min(2, sg.chunk_end - ch);  // 64-token steps in this block
                     const int s = jj % S::NS;
                     if (jj >= S::NS &&
                         !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1)) {
@@ -319,21 +335,23 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
-                    int ys[4];
-                    int rows[4];
+                    int ys[8];
+                    int rows[8];
                     int nl = 0;
-                    for (int i = 0; i < nsub; ++i) {
-                        const int tok = ch * kChunk + i * Pb;
-                        const int lp = tok / a.P;
-                        if (lp >= npages) break;
-                        const int pid = bt[lp];
-                        if (pid < 0 || pid >= a.num_pages) {
-                            report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
-                            continue;
+                    for (int hh = 0; hh < nh; ++hh) {
+                        for (int i = 0; i < nsub; ++i) {
+                            const int tok = (ch + hh) * kChunk + i * Pb;
+                            const int lp = tok / a.P;
+                            if (lp >= npages) break;
+                            const int pid = bt[lp];
+                            if (pid < 0 || pid >= a.num_pages) {
+                                report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
+                                continue;
+                            }
+                            ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok % a.P);
+                            rows[nl] = hh * kChunk + i * Pb;
+                            ++nl;
                         }
-                        ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok % a.P);
-                        rows[nl] = i * Pb;
-                        ++nl;
                     }
                     const uint32_t fb = bar(S::KV_FULL + s);
                     const uint32_t bytes = static_cast<uint32_t>(nl * Pb * 128 * S::DH * 2);
@@ -368,27 +386,27 @@ __global__ void __launch_bounds__(192, 1)
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
                    misc->x1);
-            const uint32_t idesc_qk = idesc_bf16_f32(kRows, kChunk, false, false);
+            const uint32_t idesc_qk = idesc_bf16_f32(kRows, kBlock, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
             uint32_t jj = 0, kk = 0;
             bool ok = true;
             Segment sg;
-            // O[kk&1] += P[j&1] . V[stage of j]
+            // O += P[j&1] (TMEM) . V[stage of j]
             auto issue_pv = [&](uint32_t j, bool first) -> bool {
                 if (!ptx::mbar_wait(bar(S::P_FULL + (j & 1)), (j >> 1) & 1)) return false;
-                if (first && kk >= 2 &&
-                    !ptx::mbar_wait(bar(S::O_FREE + (kk & 1)), ((kk >> 1) - 1) & 1))
+                // A segment's first P.V overwrites O: the previous epilogue
+                // must have read it.
+                if (first && kk >= 1 && !ptx::mbar_wait(bar(S::O_FREE), (kk - 1) & 1))
                     return false;
                 ptx::tc_fence_after();
                 const uint32_t vst =
                     sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
-                const uint32_t pst = sb + S::OFF_P + (j & 1) * S::PBUF_BYTES;
-                const uint32_t d_o = tmem + S::TM_O + (kk & 1) * D;
+                const uint32_t pt = tmem + S::TM_P + (j & 1) * (kBlock / 2);
+                const uint32_t d_o = tmem + S::TM_O;
 #pragma unroll
-                for (int k = 0; k < kChunk / 16; ++k) {
-                    const uint64_t ad = smem_desc_sw128(pst + k * 32, 16, 1024);
+                for (int k = 0; k < kBlock / 16; ++k) {
                     const uint64_t bd = smem_desc_sw128(vst + k * 16 * 128, S::HALF_BYTES, 1024);
-                    ptx::mma_bf16(d_o, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+                    ptx::mma_bf16_ts(d_o, pt + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
                 }
                 ptx::mma_commit(bar(S::KV_EMPTY + j % S::NS));
                 ptx::mma_commit(bar(S::P_FREE + (j & 1)));
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const int n = sg.chunk_end - sg.chunk_begin;
+                const int n = blocks_of(sg);
                 for (int p = 0; p < n; ++p, ++jj) {
                     const int s = jj % S::NS;
                     if (!ptx::mbar_wait(bar(S::KV_FULL + s), (jj / S::NS) & 1) ||
@@ -412,7 +430,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
-                    const uint32_t d_s = tmem + S::TM_S + (jj & 1) * kChunk;
+                    const uint32_t d_s = tmem + S::TM_S + (jj & 1) * kBlock;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint64_t ad = smem_desc_sw128(
@@ -435,7 +453,7 @@ __global__ void __launch_bounds__(192, 1)
                     fail();
                     break;
                 }
-                ptx::mma_commit(bar(S::O_FULL + (kk & 1)));
+                ptx::mma_commit(bar(S::O_FULL));
                 ++kk;
             }
             // Every MMA issued above must finish before TMEM is released.
@@ -444,7 +462,12 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ================= softmax + epilogue warpgroup (warps 0-3)
-        const int r = threadIdx.x;  // tile row == TMEM lane
+        constexpr int R = kRows / F;    // tile rows per replica
+        constexpr int KF = kBlock / F;  // keys of each block one replica handles
+        const int r = threadIdx.x;      // tile row == TMEM lane
+        const int g = r / R;            // replica of this row (warp-uniform)
+        const int lr = r % R;           // query row within the row block
+        const int k0 = g * KF;          // first key of this replica in a block
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         Walker w;
         w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
@@ -455,14 +478,25 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) fail();
             return all;
         };
-        // Stage Q rows of a segment into the swizzled K-major A tile.
+        // P columns outside this replica's keys must read as zero: clear both
+        // P buffers once; afterwards only the replica's own columns are written.
+        {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBlock; c += 32) ptx::tmem_st32(lane_base + S::TM_P + c, z);
+            ptx::tmem_wait_st();
+        }
+        // Stage Q rows of a segment into the swizzled K-major A tile (every
+        // replica gets a copy).
         auto load_q = [&](const Segment& sg) {
-            const int Mrb = min(kRows, a.M - sg.rb * kRows);
+            const int Mrb = min(R, a.M - sg.rb * kRows);
             uint8_t* qs = smem + S::OFF_Q;
-            if (r < Mrb) {
-                const int rr = sg.rb * kRows + r;
-                const int t = rr / a.G, g = rr % a.G;
-                const int h = sg.hk * a.G + g;
+            if (lr < Mrb) {
+                const int rr = sg.rb * kRows + lr;
+                const int t = rr / a.G, gg = rr % a.G;
+                const int h = sg.hk * a.G + gg;
                 const uint4* src = reinterpret_cast<const uint4*>(
                     a.q + ((static_cast<size_t>(sg.b) * a.T + t) * a.Hq + h) * D);
 #pragma unroll
@@ -488,57 +522,73 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
         if (have) load_q(cur);
         while (ok && have) {
-            const int Mrb = min(kRows, a.M - cur.rb * kRows);
-            const bool row_ok = r < Mrb;
-            const bool warp_any = warp * 32 < Mrb;
+            const int Mrb = min(R, a.M - cur.rb * kRows);
+            const bool row_ok = lr < Mrb;
+            const bool warp_any = (warp * 32) % R < Mrb;
             bool bad;
             const int L = clamp_seq_len(a.seq_lens[cur.b], a.P, a.max_pages, bad);
-            float m_ref = kNegInf;
+            float m_ref = kNegInf;  // base-2 reference; -inf until a key is seen
             float l_sum = 0.f;
-            for (int ch = cur.chunk_begin; ch < cur.chunk_end; ++ch, ++jj) {
+            for (int ch = cur.chunk_begin; ch < cur.chunk_end; ch += 2, ++jj) {
                 const bool first = ch == cur.chunk_begin;
-                const int n_valid = min(kChunk, L - ch * kChunk);
+                const int nh = min(2, cur.chunk_end - ch);
+                const int n_valid = min(nh * kChunk, L - ch * kChunk);
+                const int nv = n_valid - k0;  // valid keys in this replica's range (may be <= 0)
                 if (!wait_all(bar(S::S_FULL + (jj & 1)), (jj >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                float s[kChunk];
+                float s[KF];
                 if (warp_any) {
-                    const uint32_t ta = lane_base + S::TM_S + (jj & 1) * kChunk;
-                    ptx::tmem_ld32(ta, s);
-                    ptx::tmem_ld32(ta + 32, s + 32);
+                    const uint32_t ta = lane_base + S::TM_S + (jj & 1) * kBlock + k0;
+#pragma unroll
+                    for (int c = 0; c < KF; c += 32) ptx::tmem_ld32(ta + c, s + c);
                     ptx::tmem_wait_ld();
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(S::S_FREE + (jj & 1)));
 
+                // Softmax in the base-2 domain: x = s * scale * log2(e)
+                // (scale > 0, so the max of the raw scores gives the max of x).
                 float alpha = 1.f;
                 bool rescale = false;
                 if (row_ok) {
                     float mx = kNegInf;
+                    if (nv >= KF) {
 #pragma unroll
-                    for (int i = 0; i < kChunk; ++i) {
-                        const float x = (i < n_valid) ? s[i] * a.scale_log2 : kNegInf;
-                        s[i] = x;
-                        mx = fmaxf(mx, x);
+                        for (int i = 0; i < KF; ++i) mx = fmaxf(mx, s[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < KF; ++i)
+                            if (i < nv) mx = fmaxf(mx, s[i]);
                     }
+                    mx *= a.scale_log2;
                     if (first) {
                         m_ref = mx;
                     } else if (mx > m_ref + 8.f) {
                         // Keep 2^(x - m_ref) <= 2^8: move the reference and
-                        // rescale the running sums.
+                        // rescale the running sums (alpha = 0 if there were none).
                         alpha = ptx::ex2(m_ref - mx);
                         m_ref = mx;
                         l_sum *= alpha;
                         rescale = true;
                     }
+                    const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;
                     float sum = 0.f;
+                    if (nv >= KF) {
 #pragma unroll
-                    for (int i = 0; i < kChunk; ++i) {
-                        s[i] = ptx::ex2(s[i] - m_ref);
-                        sum += s[i];
+                        for (int i = 0; i < KF; ++i) {
+                            s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
+                            sum += s[i];
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < KF; ++i) {
+                            s[i] = (i < nv) ? ptx::ex2(fmaf(s[i], a.scale_log2, neg_m)) : 0.f;
+                            sum += s[i];
+                        }
                     }
                     l_sum += sum;
                 }
@@ -547,15 +597,20 @@ __global__ void __launch_bounds__(192, 1)
                     ok = false;
                     break;
                 }
-                if (row_ok) {
-                    const uint32_t pst = sb + S::OFF_P + (jj & 1) * S::PBUF_BYTES;
+                if (warp_any) {
+                    const uint32_t tp = lane_base + S::TM_P + (jj & 1) * (kBlock / 2) + k0 / 2;
+                    uint32_t pk[KF / 2];
 #pragma unroll
-                    for (int c = 0; c < kChunk / 8; ++c) {
-                        st_shared_v4(pst + sw128_offset(r, c), pack_bf16(s[8 * c], s[8 * c + 1]),
-                                     pack_bf16(s[8 * c + 2], s[8 * c + 3]),
-                                     pack_bf16(s[8 * c + 4], s[8 * c + 5]),
-                                     pack_bf16(s[8 * c + 6], s[8 * c + 7]));
+                    for (int i = 0; i < KF / 2; ++i)
+                        pk[i] = row_ok ? pack_bf16(s[2 * i], s[2 * i + 1]) : 0u;
+                    if constexpr (KF / 2 >= 32) {
+#pragma unroll
+                        for (int c = 0; c < KF / 2; c += 32)
+                            ptx::tmem_st32(tp + c, reinterpret_cast<const float*>(pk + c));
+                    } else {
+                        ptx::tmem_st16(tp, pk);
                     }
+                    ptx::tmem_wait_st();
                 }
                 if (__any_sync(kFull, rescale)) {
                     // O must hold PV(jj - 1) before it is rescaled in place.
@@ -564,7 +619,7 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t to = lane_base + S::TM_O + (kk & 1) * D;
+                    const uint32_t to = lane_base + S::TM_O;
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         float o[32];
@@ -576,7 +631,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     ptx::tmem_wait_st();
                 }
-                if (n_valid < kChunk) {
+                if (n_valid < kBlock) {
                     // Slots past the sequence end hold stale data; zero their
                     // V rows so 0 * garbage cannot reach O.
                     if (!wait_all(bar(S::KV_FULL + jj % S::NS), (jj / S::NS) & 1)) {
@@ -585,15 +640,15 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t vst =
                         sb + S::OFF_STAGE + (jj % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
-                    const int items = (kChunk - n_valid) * S::DH * 8;
+                    const int items = (kBlock - n_valid) * S::DH * 8;
                     for (int it = r; it < items; it += 128) {
                         const int row = n_valid + it / (S::DH * 8);
                         const int rem = it % (S::DH * 8);
                         st_shared_v4(vst + (rem >> 3) * S::HALF_BYTES + row * 128 + (rem & 7) * 16,
                                      0u, 0u, 0u, 0u);
                     }
+                    ptx::fence_proxy_async_smem();
                 }
-                ptx::fence_proxy_async_smem();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(S::P_FULL + (jj & 1)));
@@ -604,14 +659,14 @@ __global__ void __launch_bounds__(192, 1)
             Segment nxt;
             const bool have_next = w.next(nxt);
             if (have_next) load_q(nxt);
-            if (!wait_all(bar(S::O_FULL + (kk & 1)), (kk >> 1) & 1)) {
+            if (!wait_all(bar(S::O_FULL), kk & 1)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             if (warp_any) {
                 float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
-                const uint32_t to = lane_base + S::TM_O + (kk & 1) * D;
+                const uint32_t to = lane_base + S::TM_O;
                 float4* acc =
                     reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
 #pragma unroll
@@ -633,7 +688,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(S::O_FREE + (kk & 1)));
+            if (lane == 0) ptx::mbar_arrive(bar(S::O_FREE));
             ++kk;
             cur = nxt;
             have = have_next;
@@ -789,29 +844,34 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
     ptx::grid_dep_launch();
     if (!active) return;
     const size_t sf = static_cast<size_t>(slot_floats(D));
-    const float* wsr = a.ws + r;  // row r of slot 0
-    const int nslots = c_last - c_first + 1;
-    // First round trip: (m, l) of up to 32 slots (lane j: slot c_first + j)
-    // and the accumulator rows of the first eight slots, all issued before
-    // any of them is used.  Partials are read through L2 only
-    // (ld.global.cg): the prefix grid wrote them while this grid was resident.
+    // Partials are indexed by "virtual slot" v: prefix CTA c = c_first + v / F
+    // and query-row copy g = v % F of that CTA's tile (rows g * R + r).
+    const int F = a.RB == 1 ? replicas_of(a.M) : 1;
+    const int R = kRows / F;
+    const int nv = (c_last - c_first + 1) * F;
+    auto v_m = [&](int v) -> size_t {  // offset of m for virtual slot v
+        return static_cast<size_t>(unit + c_first + v / F) * sf + (v % F) * R + r;
+    };
+    auto v_acc = [&](int v) -> size_t {  // offset of this lane's accumulator values
+        return static_cast<size_t>(unit + c_first + v / F) * sf + 2 * kRows +
+               static_cast<size_t>((v % F) * R + r) * D + lane * E;
+    };
+    auto v_work = [&](int v) -> bool { return cta_has_work(c_first + v / F, W, a.n_ctas); };
+    // First round trip: (m, l) of up to 32 virtual slots (lane j: slot j)
+    // and the accumulator rows of the first eight, all issued before any of
+    // them is used.  Partials are read through L2 only (ld.global.cg): the
+    // prefix grid wrote them while this grid was resident.
     float m_j = kNegInf, l_j = 0.f;
-    if (lane < nslots && cta_has_work(c_first + lane, W, a.n_ctas)) {
-        const float* slot = wsr + (unit + c_first + lane) * sf;
-        m_j = __ldcg(slot);
-        l_j = __ldcg(slot + kRows);
+    if (lane < nv && v_work(lane)) {
+        m_j = __ldcg(a.ws + v_m(lane));
+        l_j = __ldcg(a.ws + v_m(lane) + kRows);
     }
     float v[8][E];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const bool use = j < nslots && cta_has_work(c_first + j, W, a.n_ctas);
-        load_acc<E>(a.ws + (unit + c_first + j) * sf + 2 * kRows + static_cast<size_t>(r) * D +
-                        lane * E,
-                    use, v[j]);
-    }
+    for (int j = 0; j < 8; ++j) load_acc<E>(a.ws + v_acc(j), j < nv && v_work(j), v[j]);
     float mx = fmaxf(m_s, m_j);
-    for (int c = c_first + 32 + lane; c <= c_last; c += 32)  // rare: > 32 slots
-        if (cta_has_work(c, W, a.n_ctas)) mx = fmaxf(mx, __ldcg(wsr + (unit + c) * sf));
+    for (int vv = 32 + lane; vv < nv; vv += 32)  // rare: more than 32 partials
+        if (v_work(vv)) mx = fmaxf(mx, __ldcg(a.ws + v_m(vv)));
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
     uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
     float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
@@ -833,28 +893,26 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
     }
-    // Remaining slots, eight accumulator rows per round trip.
-    for (int c0 = c_first; c0 <= c_last; c0 += 32) {
-        if (c0 != c_first) {
-            const int c = c0 + lane;
+    // Remaining partials, eight accumulator rows per round trip.
+    for (int v0 = 0; v0 < nv; v0 += 32) {
+        if (v0 != 0) {
+            const int vv = v0 + lane;
             wc = 0.f;
             float lc = 0.f;
-            if (c <= c_last && cta_has_work(c, W, a.n_ctas)) {
-                const float* slot = wsr + (unit + c) * sf;
-                wc = ptx::ex2(__ldcg(slot) - mx);
-                lc = __ldcg(slot + kRows);
+            if (vv < nv && v_work(vv)) {
+                const float mm = __ldcg(a.ws + v_m(vv));
+                wc = (mm == kNegInf) ? 0.f : ptx::ex2(mm - mx);
+                lc = __ldcg(a.ws + v_m(vv) + kRows);
             }
             total += warp_sum(wc * lc);
         }
-        const int nb = min(32, c_last - c0 + 1);
-        for (int j0 = (c0 == c_first) ? 8 : 0; j0 < nb; j0 += 8) {
+        const int nb = min(32, nv - v0);
+        for (int j0 = (v0 == 0) ? 8 : 0; j0 < nb; j0 += 8) {
             float wj[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 wj[j] = __shfl_sync(kFull, wc, j0 + j);
-                load_acc<E>(a.ws + (unit + c0 + j0 + j) * sf + 2 * kRows +
-                                static_cast<size_t>(r) * D + lane * E,
-                            j0 + j < nb && wj[j] != 0.f, v[j]);
+                load_acc<E>(a.ws + v_acc(v0 + j0 + j), j0 + j < nb && wj[j] != 0.f, v[j]);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -899,9 +957,10 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(prefix_pass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 S::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
+        for (auto k : {prefix_pass_kernel<D, 1>, prefix_pass_kernel<D, 2>, prefix_pass_kernel<D, 4>}) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+        }
         configured_for = dev;
     }
     const int G = v.Hq / v.Hkv;
@@ -926,8 +985,10 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.scale_log2 = v.scale_log2;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
-    return launch_pdl(prefix_pass_kernel<D>, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk,
-                      tv, pa);
+    const int F = pa.RB == 1 ? replicas_of(M) : 1;
+    auto kernel = F == 4 ? prefix_pass_kernel<D, 4>
+                         : (F == 2 ? prefix_pass_kernel<D, 2> : prefix_pass_kernel<D, 1>);
+    return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, pa);
 }
 
 template <int D>

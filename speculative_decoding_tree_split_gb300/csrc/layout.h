@@ -194,6 +194,14 @@ inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, in
     }
 }
 
+// Query-row replication in the prefix pass.  With few query rows per unit
+// the 128-row tile holds F copies of them; copy g sits at tile rows
+// [g*128/F, (g+1)*128/F) and handles keys [g*128/F, (g+1)*128/F) of every
+// 128-key block, so all four softmax warps share the exponentials.  Each copy
+// keeps its own (m, l, acc), stored in its own rows of the partial slot.
+// Units with more than 128 query rows are split into row blocks (F = 1).
+TA_HD int replicas_of(int M) { return M <= 32 ? 4 : (M <= 64 ? 2 : 1); }
+
 // Partial-result slot layout: m[kRows] | l[kRows] | acc[kRows][d] (fp32).
 TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>(kRows) * d; }
 
