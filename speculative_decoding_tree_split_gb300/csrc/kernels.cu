@@ -382,36 +382,18 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 5) {
         // ================= MMA issuer (one thread)
+        // Issues S = Q.K^T for the next block as soon as its K/V has landed
+        // and P.V for the oldest block as soon as its P is ready, whichever
+        // comes first, so neither waits behind the other.
         if (lane == 0) {
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
                    misc->x1);
             const uint32_t idesc_qk = idesc_bf16_f32(kRows, kBlock, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
-            uint32_t jj = 0, kk = 0;
+            uint32_t jj = 0, kk = 0;  // blocks of earlier segments, segments done
             bool ok = true;
             Segment sg;
-            // O += P[j&1] (TMEM) . V[stage of j]
-            auto issue_pv = [&](uint32_t j, bool first) -> bool {
-                if (!ptx::mbar_wait(bar(S::P_FULL + (j & 1)), (j >> 1) & 1)) return false;
-                // A segment's first P.V overwrites O: the previous epilogue
-                // must have read it.
-                if (first && kk >= 1 && !ptx::mbar_wait(bar(S::O_FREE), (kk - 1) & 1))
-                    return false;
-                ptx::tc_fence_after();
-                const uint32_t vst =
-                    sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
-                const uint32_t pt = tmem + S::TM_P + (j & 1) * (kBlock / 2);
-                const uint32_t d_o = tmem + S::TM_O;
-#pragma unroll
-                for (int k = 0; k < kBlock / 16; ++k) {
-                    const uint64_t bd = smem_desc_sw128(vst + k * 16 * 128, S::HALF_BYTES, 1024);
-                    ptx::mma_bf16_ts(d_o, pt + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
-                }
-                ptx::mma_commit(bar(S::KV_EMPTY + j % S::NS));
-                ptx::mma_commit(bar(S::P_FREE + (j & 1)));
-                return true;
-            };
             while (ok && w.next(sg)) {
                 if (!ptx::mbar_wait(bar(S::Q_FULL), kk & 1)) {
                     fail();
@@ -419,41 +401,73 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 ptx::tc_fence_after();
                 const int n = blocks_of(sg);
-                for (int p = 0; p < n; ++p, ++jj) {
-                    const int s = jj % S::NS;
-                    if (!ptx::mbar_wait(bar(S::KV_FULL + s), (jj / S::NS) & 1) ||
-                        (jj >= 2 &&
-                         !ptx::mbar_wait(bar(S::S_FREE + (jj & 1)), ((jj >> 1) - 1) & 1)) ||
-                        *abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
-                    const uint32_t d_s = tmem + S::TM_S + (jj & 1) * kBlock;
+                int nq = 0, np = 0;  // S MMAs / P.V MMAs issued in this segment
+                uint64_t t0 = 0;
+                while (np < n) {
+                    bool progress = false;
+                    // P.V for block np once P is ready (and, for the first
+                    // block, once the previous epilogue has read O).
+                    if (np < nq) {
+                        const uint32_t j = jj + np;
+                        if (ptx::mbar_try_wait(bar(S::P_FULL + (j & 1)), (j >> 1) & 1) &&
+                            (np > 0 || kk == 0 || ptx::mbar_try_wait(bar(S::O_FREE), (kk - 1) & 1))) {
+                            ptx::tc_fence_after();
+                            const uint32_t vst =
+                                sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
+                            const uint32_t pt = tmem + S::TM_P + (j & 1) * (kBlock / 2);
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t ad = smem_desc_sw128(
-                            sb + S::OFF_Q + (k >> 2) * S::QATOM_BYTES + (k & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(
-                            kst + (k >> 2) * S::HALF_BYTES + (k & 3) * 32, 16, 1024);
-                        ptx::mma_bf16(d_s, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                            for (int k = 0; k < kBlock / 16; ++k) {
+                                const uint64_t bd =
+                                    smem_desc_sw128(vst + k * 16 * 128, S::HALF_BYTES, 1024);
+                                ptx::mma_bf16_ts(tmem + S::TM_O, pt + k * 8, bd, idesc_pv,
+                                                 (np == 0 && k == 0) ? 0u : 1u);
+                            }
+                            ptx::mma_commit(bar(S::KV_EMPTY + j % S::NS));
+                            ptx::mma_commit(bar(S::P_FREE + (j & 1)));
+                            ++np;
+                            progress = true;
+                        }
                     }
-                    ptx::mma_commit(bar(S::S_FULL + (jj & 1)));
-                    if (p > 0 && !issue_pv(jj - 1, p == 1)) {
-                        ok = false;
-                        break;
+                    // S for block nq once its K/V has landed and its S buffer
+                    // has been read by the softmax (block nq - 2).
+                    if (nq < n) {
+                        const uint32_t j = jj + nq;
+                        const int s = j % S::NS;
+                        if (ptx::mbar_try_wait(bar(S::KV_FULL + s), (j / S::NS) & 1) &&
+                            (j < 2 || ptx::mbar_try_wait(bar(S::S_FREE + (j & 1)), ((j >> 1) - 1) & 1))) {
+                            ptx::tc_fence_after();
+                            const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
+                            const uint32_t d_s = tmem + S::TM_S + (j & 1) * kBlock;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint64_t ad = smem_desc_sw128(
+                                    sb + S::OFF_Q + (k >> 2) * S::QATOM_BYTES + (k & 3) * 32, 16, 1024);
+                                const uint64_t bd = smem_desc_sw128(
+                                    kst + (k >> 2) * S::HALF_BYTES + (k & 3) * 32, 16, 1024);
+                                ptx::mma_bf16(d_s, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+                            }
+                            ptx::mma_commit(bar(S::S_FULL + (j & 1)));
+                            ++nq;
+                            progress = true;
+                        }
+                    }
+                    if (progress) {
+                        t0 = 0;
+                    } else {
+                        const uint64_t now = ptx::globaltimer();
+                        if (t0 == 0) t0 = now;
+                        if (now - t0 > ptx::kWaitLimitNs || *abort_flag) {
+                            ok = false;
+                            break;
+                        }
                     }
                 }
                 if (!ok) {
                     fail();
                     break;
                 }
-                if (!issue_pv(jj - 1, n == 1)) {
-                    fail();
-                    break;
-                }
                 ptx::mma_commit(bar(S::O_FULL));
+                jj += n;
                 ++kk;
             }
             // Every MMA issued above must finish before TMEM is released.
@@ -555,15 +569,21 @@ __global__ void __launch_bounds__(192, 1)
                 float alpha = 1.f;
                 bool rescale = false;
                 if (row_ok) {
-                    float mx = kNegInf;
+                    // Eight independent partial maxima / sums keep the
+                    // dependency chains short.
+                    float mp[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mp[u] = kNegInf;
                     if (nv >= KF) {
 #pragma unroll
-                        for (int i = 0; i < KF; ++i) mx = fmaxf(mx, s[i]);
+                        for (int i = 0; i < KF; ++i) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < KF; ++i)
-                            if (i < nv) mx = fmaxf(mx, s[i]);
+                            if (i < nv) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
                     }
+                    float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
                     mx *= a.scale_log2;
                     if (first) {
                         m_ref = mx;
@@ -576,21 +596,23 @@ __global__ void __launch_bounds__(192, 1)
                         rescale = true;
                     }
                     const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;
-                    float sum = 0.f;
+                    float sp[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) sp[u] = 0.f;
                     if (nv >= KF) {
 #pragma unroll
                         for (int i = 0; i < KF; ++i) {
                             s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
-                            sum += s[i];
+                            sp[i & 7] += s[i];
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < KF; ++i) {
                             s[i] = (i < nv) ? ptx::ex2(fmaf(s[i], a.scale_log2, neg_m)) : 0.f;
-                            sum += s[i];
+                            sp[i & 7] += s[i];
                         }
                     }
-                    l_sum += sum;
+                    l_sum += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
                 }
                 // P buffer (jj & 1) is free once PV(jj - 2) has completed.
                 if (jj >= 2 && !wait_all(bar(S::P_FREE + (jj & 1)), ((jj >> 1) - 1) & 1)) {
@@ -719,6 +741,7 @@ struct MergeArgs {
     uint16_t* out;
     float* lse;
     int B, Hq, Hkv, G, T, M, RB, P, max_pages, n_ctas;
+    int wpr;  // warps per query row in the merge (1, 2, 4 or 8)
     float scale_log2;
 };
 
@@ -764,69 +787,53 @@ __device__ __forceinline__ void load_acc(const float* p, bool use, float* v) {
     }
 }
 
-constexpr int kMergeRows = 8;  // rows (warps) per CTA
+constexpr int kMergeWarps = 4;  // warps per CTA
 
-template <int D>
-__global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const MergeArgs a) {
+// One CTA = 4 warps = 4 / wpr query rows; the wpr warps of a row split its
+// partials (virtual slot v goes to warp v % wpr) and combine through shared
+// memory.  Every independent load of a phase is issued before any of its
+// results is used, so each phase costs about one memory round trip.
+template <int D, int F>
+__global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const MergeArgs a) {
     constexpr int E = D / 32;
+    constexpr int R = kRows / F;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int wpr = a.wpr;
+    const int rows_per_cta = kMergeWarps / wpr;
+    const int wr = warp / wpr;   // row slot of this warp in the CTA
+    const int sub = warp % wpr;  // this warp's share of the row's partials
     const int unit = blockIdx.x;
     const int rb = unit % a.RB;
     const int hk = (unit / a.RB) % a.Hkv;
     const int b = unit / (a.RB * a.Hkv);
-    const int r = blockIdx.y * kMergeRows + warp;
+    const int r = blockIdx.y * rows_per_cta + wr;
     const int rr = rb * kRows + r;
     const bool active = r < kRows && rr < a.M;
 
-    // ---- suffix: online softmax over the tree keys mask[t] allows.  Reads
-    // only inputs of this call, so it runs before waiting for the prefix pass.
-    float m_s = kNegInf, l_s = 0.f;
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    __shared__ float red_m[kMergeWarps];
+    __shared__ float red_l[kMergeWarps];
+    __shared__ float red_o[kMergeWarps][D];
+
     int t = 0, h = 0;
     if (active) {
         t = rr / a.G;
         h = hk * a.G + rr % a.G;
-        float qv[E];
-        load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
-        uint64_t bits = a.mask[t];
-        if (a.T < 64) bits &= (1ull << a.T) - 1ull;
-        while (bits != 0) {
-            const int j = __ffsll(static_cast<long long>(bits)) - 1;
-            bits &= bits - 1;
-            const size_t off = ((static_cast<size_t>(b) * a.T + j) * a.Hkv + hk) * D + lane * E;
-            float kv[E], vv[E];
-            load_bf16<E>(a.tree_k + off, kv);
-            load_bf16<E>(a.tree_v + off, vv);
-            float dot = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
-            const float x = warp_sum(dot) * a.scale_log2;
-            const float mn = fmaxf(m_s, x);
-            const float al = ptx::ex2(m_s - mn);
-            const float p = ptx::ex2(x - mn);
-            l_s = l_s * al + p;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[e], acc[e] * al);
-            m_s = mn;
-        }
     }
 
-    // ---- where this unit's prefix partials live (inputs only, so this also
-    // runs before the prefix pass has finished)
+    // ---- work-line plan of this unit (inputs only): sequence lengths of
+    // the whole batch, loaded 64 at a time.
     const int upb = a.Hkv * a.RB;
     long long W = 0, base_b = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-        const int bb = b0 + lane;
-        int n = 0;
-        if (bb < a.B) {
-            bool bad;
-            n = chunks_of(clamp_seq_len(a.seq_lens[bb], a.P, a.max_pages, bad));
-        }
-        W += __reduce_add_sync(kFull, n);
-        base_b += __reduce_add_sync(kFull, bb < b ? n : 0);
+    for (int b0 = 0; b0 < a.B; b0 += 64) {
+        const int b1 = b0 + lane, b2 = b0 + 32 + lane;
+        const int32_t l1 = b1 < a.B ? a.seq_lens[b1] : 0;
+        const int32_t l2 = b2 < a.B ? a.seq_lens[b2] : 0;
+        bool bad;
+        const int n1 = b1 < a.B ? chunks_of(clamp_seq_len(l1, a.P, a.max_pages, bad)) : 0;
+        const int n2 = b2 < a.B ? chunks_of(clamp_seq_len(l2, a.P, a.max_pages, bad)) : 0;
+        W += __reduce_add_sync(kFull, n1 + n2);
+        base_b += __reduce_add_sync(kFull, (b1 < b ? n1 : 0) + (b2 < b ? n2 : 0));
     }
     W *= upb;
     base_b *= upb;
@@ -839,16 +846,82 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
         c_last = cta_of(ustart + nch - 1, W, a.n_ctas);
     }
 
+    // ---- suffix (sub-warp 0 of each row): softmax over the tree keys
+    // mask[t] allows, four keys per round trip.  Reads only inputs of this
+    // call, so it runs before waiting for the prefix pass.
+    float m_s = kNegInf, l_s = 0.f;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (active && sub == 0) {
+        float qv[E];
+        load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
+        uint64_t bits = a.mask[t];
+        if (a.T < 64) bits &= (1ull << a.T) - 1ull;
+        while (bits != 0) {
+            int js[4];
+            int n = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                js[i] = 0;
+                if (bits != 0) {
+                    js[i] = __ffsll(static_cast<long long>(bits)) - 1;
+                    bits &= bits - 1;
+                    n = i + 1;
+                }
+            }
+            float kv[4][E], vv[4][E];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < n) {
+                    const size_t off =
+                        ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
+                    load_bf16<E>(a.tree_k + off, kv[i]);
+                    load_bf16<E>(a.tree_v + off, vv[i]);
+                }
+            }
+            float x[4];
+            float mx = m_s;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float dot = 0.f;
+                if (i < n) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[i][e], dot);
+                }
+                x[i] = warp_sum(dot) * a.scale_log2;
+                if (i < n) mx = fmaxf(mx, x[i]);
+            }
+            const float al = ptx::ex2(m_s - mx);
+            l_s *= al;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] *= al;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < n) {
+                    const float p = ptx::ex2(x[i] - mx);
+                    l_s += p;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[i][e], acc[e]);
+                }
+            }
+            m_s = mx;
+        }
+    }
+
     // ---- merge with the partials of the prefix pass
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
-    if (!active) return;
     const size_t sf = static_cast<size_t>(slot_floats(D));
     // Partials are indexed by "virtual slot" v: prefix CTA c = c_first + v / F
-    // and query-row copy g = v % F of that CTA's tile (rows g * R + r).
-    const int F = a.RB == 1 ? replicas_of(a.M) : 1;
-    const int R = kRows / F;
-    const int nv = (c_last - c_first + 1) * F;
+    // and query-row copy g = v % F of that CTA's tile (rows g * R + r).  This
+    // warp takes v = sub, sub + wpr, ...; its k-th one is v = sub + k * wpr.
+    const int nv = active ? (c_last - c_first + 1) * F : 0;
+    const int nmine = nv > sub ? (nv - sub + wpr - 1) / wpr : 0;
+    // With at least one work-line step per CTA every CTA in [c_first, c_last]
+    // wrote a partial; only when W < C can some of them be empty.
+    const bool every_cta = W >= a.n_ctas;
+    auto v_of = [&](int k) -> int { return sub + k * wpr; };
     auto v_m = [&](int v) -> size_t {  // offset of m for virtual slot v
         return static_cast<size_t>(unit + c_first + v / F) * sf + (v % F) * R + r;
     };
@@ -856,69 +929,92 @@ __global__ void __launch_bounds__(32 * kMergeRows) suffix_merge_kernel(const Mer
         return static_cast<size_t>(unit + c_first + v / F) * sf + 2 * kRows +
                static_cast<size_t>((v % F) * R + r) * D + lane * E;
     };
-    auto v_work = [&](int v) -> bool { return cta_has_work(c_first + v / F, W, a.n_ctas); };
-    // First round trip: (m, l) of up to 32 virtual slots (lane j: slot j)
-    // and the accumulator rows of the first eight, all issued before any of
-    // them is used.  Partials are read through L2 only (ld.global.cg): the
-    // prefix grid wrote them while this grid was resident.
+    auto v_work = [&](int v) -> bool {
+        return every_cta || cta_has_work(c_first + v / F, W, a.n_ctas);
+    };
+    // One round trip: (m, l) of this warp's first 32 partials (lane k: the
+    // k-th) and the accumulator rows of its first four.  Partials are read
+    // through L2 only (ld.global.cg): the prefix grid wrote them while this
+    // grid was resident.
     float m_j = kNegInf, l_j = 0.f;
-    if (lane < nv && v_work(lane)) {
-        m_j = __ldcg(a.ws + v_m(lane));
-        l_j = __ldcg(a.ws + v_m(lane) + kRows);
+    if (lane < nmine && v_work(v_of(lane))) {
+        m_j = __ldcg(a.ws + v_m(v_of(lane)));
+        l_j = __ldcg(a.ws + v_m(v_of(lane)) + kRows);
     }
-    float v[8][E];
+    float v[4][E];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) load_acc<E>(a.ws + v_acc(j), j < nv && v_work(j), v[j]);
+    for (int j = 0; j < 4; ++j)
+        load_acc<E>(a.ws + v_acc(v_of(j)), j < nmine && v_work(v_of(j)), v[j]);
     float mx = fmaxf(m_s, m_j);
-    for (int vv = 32 + lane; vv < nv; vv += 32)  // rare: more than 32 partials
-        if (v_work(vv)) mx = fmaxf(mx, __ldcg(a.ws + v_m(vv)));
+    for (int k = 32 + lane; k < nmine; k += 32)  // rare: more than 32 partials per warp
+        if (v_work(v_of(k))) mx = fmaxf(mx, __ldcg(a.ws + v_m(v_of(k))));
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
-    float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
-    if (mx == kNegInf) {  // no key at all
-#pragma unroll
-        for (int e = 0; e < E; ++e) op[e] = 0;
-        if (lane == 0) *lp = kNegInf;
-        return;
+    if (wpr > 1) {
+        if (lane == 0) red_m[warp] = mx;
+        __syncthreads();
+        for (int s2 = 0; s2 < wpr; ++s2) mx = fmaxf(mx, red_m[wr * wpr + s2]);
     }
-    const float w_s = ptx::ex2(m_s - mx);
+    const bool has_keys = mx != kNegInf;
+    const float w_s = has_keys ? ptx::ex2(m_s - mx) : 0.f;
     float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = acc[e] * w_s;
-    float wc = (m_j == kNegInf) ? 0.f : ptx::ex2(m_j - mx);
+    float wc = (m_j == kNegInf || !has_keys) ? 0.f : ptx::ex2(m_j - mx);
     float total = l_s * w_s + warp_sum(wc * l_j);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
         const float wj = __shfl_sync(kFull, wc, j);
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
     }
-    // Remaining partials, eight accumulator rows per round trip.
-    for (int v0 = 0; v0 < nv; v0 += 32) {
-        if (v0 != 0) {
-            const int vv = v0 + lane;
+    // Remaining partials of this warp, four accumulator rows per round trip.
+    for (int k0 = 0; k0 < nmine; k0 += 32) {
+        if (k0 != 0) {
+            const int k = k0 + lane;
             wc = 0.f;
             float lc = 0.f;
-            if (vv < nv && v_work(vv)) {
-                const float mm = __ldcg(a.ws + v_m(vv));
+            if (k < nmine && v_work(v_of(k))) {
+                const float mm = __ldcg(a.ws + v_m(v_of(k)));
                 wc = (mm == kNegInf) ? 0.f : ptx::ex2(mm - mx);
-                lc = __ldcg(a.ws + v_m(vv) + kRows);
+                lc = __ldcg(a.ws + v_m(v_of(k)) + kRows);
             }
             total += warp_sum(wc * lc);
         }
-        const int nb = min(32, nv - v0);
-        for (int j0 = (v0 == 0) ? 8 : 0; j0 < nb; j0 += 8) {
-            float wj[8];
+        const int nb = min(32, nmine - k0);
+        for (int j0 = (k0 == 0) ? 4 : 0; j0 < nb; j0 += 4) {
+            float wj[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 wj[j] = __shfl_sync(kFull, wc, j0 + j);
-                load_acc<E>(a.ws + v_acc(v0 + j0 + j), j0 + j < nb && wj[j] != 0.f, v[j]);
+                load_acc<E>(a.ws + v_acc(v_of(k0 + j0 + j)), j0 + j < nb && wj[j] != 0.f, v[j]);
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int e = 0; e < E; ++e) o[e] = fmaf(wj[j], v[j][e], o[e]);
         }
+    }
+    if (wpr > 1) {
+        // Combine the row's warps (all use the same row max mx).
+        if (lane == 0) red_l[warp] = total;
+#pragma unroll
+        for (int e = 0; e < E; ++e) red_o[warp][lane * E + e] = o[e];
+        __syncthreads();
+        if (sub != 0) return;
+        for (int s2 = 1; s2 < wpr; ++s2) {
+            total += red_l[warp + s2];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] += red_o[warp + s2][lane * E + e];
+        }
+    }
+    if (!active) return;
+    uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
+    float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
+    if (!has_keys) {  // no key at all
+#pragma unroll
+        for (int e = 0; e < E; ++e) op[e] = 0;
+        if (lane == 0) *lp = kNegInf;
+        return;
     }
     const float inv = 1.f / total;
     if constexpr (E == 4) {
@@ -1016,9 +1112,18 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.max_pages = v.max_pages;
     ma.n_ctas = v.n_ctas;
     ma.scale_log2 = v.scale_log2;
+    // Warps per row from the expected partials per row: prefix CTAs per unit
+    // (plus one for a straddled boundary) times the row copies.
+    const long long units = static_cast<long long>(v.B) * v.Hkv * RB;
+    const int F = RB == 1 ? replicas_of(M) : 1;
+    const long long expect = (v.n_ctas / units + 2) * F;
+    ma.wpr = expect > 12 ? 4 : (expect > 6 ? 2 : 1);
     const int rows = M < kRows ? M : kRows;
-    const dim3 grid(v.B * v.Hkv * RB, (rows + kMergeRows - 1) / kMergeRows);
-    return launch_pdl(suffix_merge_kernel<D>, grid, dim3(32 * kMergeRows), 0, stream, ma);
+    const int rows_per_cta = kMergeWarps / ma.wpr;
+    const dim3 grid(static_cast<unsigned>(units), (rows + rows_per_cta - 1) / rows_per_cta);
+    auto kernel = F == 4 ? suffix_merge_kernel<D, 4>
+                         : (F == 2 ? suffix_merge_kernel<D, 2> : suffix_merge_kernel<D, 1>);
+    return launch_pdl(kernel, grid, dim3(32 * kMergeWarps), 0, stream, ma);
 }
 
 }  // namespace
