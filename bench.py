@@ -45,7 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the prefix-pass
 # kernel from an ncu capture, keyed by workload, valid only for the kernel
 # source whose SHA-256 is recorded with it (see profiles/).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # Llama-3.1-8B layer, mean of three launches of one ncu capture
+    "llama8b": ("7ed6147ffaa6b3b9", 33740800),
+}
 
 
 def parse_args():
@@ -168,6 +171,19 @@ def smi_gpu_id(props, local):
     if local < len(ids):
         return ids[local].strip()
     return str(local)
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks (identity when not
+    distributed); the device follows the process group's backend."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    if device is None:
+        device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
 
 
 def emit(obj):
@@ -339,11 +355,7 @@ def run_ours(args):
 
     ms_step = ms_total / K
     ms_prefix = ms_prefix_total / K
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step, ms_prefix], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_prefix = float(t[0]), float(t[1])
+    ms_step, ms_prefix = max_over_ranks([ms_step, ms_prefix], dev)
     tokens_per_step = cfg.B * cfg.T * world
     value = tokens_per_step / (ms_step * 1e-3)
 
@@ -390,11 +402,7 @@ def run_ours(args):
         e.record()
         torch.cuda.synchronize()
         ms_e2e = s.elapsed_time(e) / n_e2e
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t[0])
+        ms_e2e = max_over_ranks([ms_e2e], dev)[0]
         e2e = {"value": tokens_per_step / (ms_e2e * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": ms_e2e}
