@@ -60,8 +60,10 @@ __device__ __forceinline__ int pick32(int lo, int hi, int node) {
 __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
                                                        uint64_t* __restrict__ mask,
                                                        int32_t* status) {
-    ptx::grid_dep_wait();
+    // The next kernel may start its prologue now; it waits for this grid
+    // before reading anything this grid writes.
     ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
     const int lane = threadIdx.x;
     int jump[2];
     uint64_t anc[2];
@@ -810,6 +812,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     const int r = blockIdx.y * rows_per_cta + wr;
     const int rr = rb * kRows + r;
     const bool active = r < kRows && rr < a.M;
+    // The next kernel may start its prologue once every CTA of this grid is
+    // running; it waits for this grid before reading anything it writes.
+    ptx::grid_dep_launch();
 
     __shared__ float red_m[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
@@ -911,7 +916,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
 
     // ---- merge with the partials of the prefix pass
     ptx::grid_dep_wait();
-    ptx::grid_dep_launch();
     const size_t sf = static_cast<size_t>(slot_floats(D));
     // Partials are indexed by "virtual slot" v: prefix CTA c = c_first + v / F
     // and query-row copy g = v % F of that CTA's tile (rows g * R + r).  This

@@ -282,3 +282,13 @@ def test_full_size_configs(oracle, name):
     got_l = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert np.abs(got_o - ref_o).max() <= OUT_TOL
     assert np.abs(got_l - ref_l).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("T,G,n_ctas", [(4, 4, 2), (8, 4, 3), (12, 4, 2), (16, 4, 2), (20, 4, 1),
+                                        (16, 5, 2)])
+def test_row_replication_paths(oracle, T, G, n_ctas):
+    # Few CTAs => many steps per CTA => the prefix pass replicates the query
+    # rows 4x (M <= 32) or 2x (M <= 64); M > 64 uses one copy.
+    cfg = Config(f"rep{T}x{G}", B=2, Hq=2 * G, Hkv=2, d=128, L=(0, 1000), page=64, T=T,
+                 max_depth=5, max_branch=4, seed=40 + T)
+    compare_all(oracle, make_workload(cfg, seq_lens=[997, 650]), n_ctas=n_ctas)
