@@ -84,6 +84,16 @@ TREE_ATTN_API int tree_mask_build(const int32_t *parents, int T, uint64_t *mask_
                                   int32_t *status, void *stream);
 
 /*
+ * tree_mask_build_batched -- tree_mask_build for n_trees trees at once
+ * (one warp each): parents int32 [n_trees][T] -> mask_out uint64
+ * [n_trees][T].  Used with per-sequence draft trees (the pages' tree
+ * dispatcher picks trees per batch; sequences may also carry their own).
+ * n_trees = 0 enqueues nothing.  Return codes as tree_mask_build.
+ */
+TREE_ATTN_API int tree_mask_build_batched(const int32_t *parents, int T, int n_trees,
+                                          uint64_t *mask_out, int32_t *status, void *stream);
+
+/*
  * tree_attn_workspace_size -- bytes of device scratch tree_attn_verify needs
  * for these sizes on the CURRENT device (the count depends on its SM count).
  * Holds the per-split partial results (m, l, acc) of the prefix pass.
@@ -161,6 +171,41 @@ TREE_ATTN_API int tree_attn_verify_ctas(const uint16_t *q, const uint16_t *k_pag
 
 TREE_ATTN_API size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T,
                                                    int page_size, int n_ctas);
+
+/*
+ * tree_attn_verify_batched -- tree_attn_verify with one draft tree per
+ * sequence: masks is uint64 [B][T] (tree b at masks[b * T], e.g. from
+ * tree_mask_build_batched).  Everything else as tree_attn_verify.
+ */
+TREE_ATTN_API int tree_attn_verify_batched(const uint16_t *q, const uint16_t *k_pages,
+                                           const uint16_t *v_pages, const int32_t *block_table,
+                                           int max_pages_per_seq, const int32_t *seq_lens,
+                                           const uint16_t *tree_k, const uint16_t *tree_v,
+                                           const uint64_t *masks, uint16_t *out, float *lse,
+                                           int B, int Hq, int Hkv, int d, int T, int page_size,
+                                           int num_pages, float softmax_scale, void *workspace,
+                                           size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
+ * tree_attn_verify_paged_tree -- split tree attention with the draft tokens
+ * padded into the paged KV cache ("paged KV with tree padding", pith.science
+ * verdict record, desk editor's note): tree token j of sequence b has its
+ * K/V at logical position seq_lens[b] + j of that sequence's pages, so the
+ * block table must cover seq_lens[b] + T tokens (else status
+ * TREE_ATTN_STATUS_BAD_SEQ_LEN).  The prefix pass covers positions
+ * [0, seq_lens[b]) unmasked; the suffix pass reads the T tree positions
+ * through the block table under the mask.  mask is uint64 [T]
+ * (mask_stride 0) or [B][T] (mask_stride T).  No tree_k / tree_v.  Other
+ * arguments, layouts and return codes as tree_attn_verify.
+ */
+TREE_ATTN_API int tree_attn_verify_paged_tree(const uint16_t *q, const uint16_t *k_pages,
+                                              const uint16_t *v_pages, const int32_t *block_table,
+                                              int max_pages_per_seq, const int32_t *seq_lens,
+                                              const uint64_t *mask, int mask_stride, uint16_t *out,
+                                              float *lse, int B, int Hq, int Hkv, int d, int T,
+                                              int page_size, int num_pages, float softmax_scale,
+                                              void *workspace, size_t workspace_bytes,
+                                              int32_t *status, void *stream);
 
 /*
  * tree_attn_prefix_pass / tree_attn_suffix_merge -- the two passes of

@@ -21,9 +21,12 @@ from ._lib import (  # noqa: F401
     TreeAttnError,
     load,
     mask_build,
+    mask_build_batched,
     prefix_pass,
     suffix_merge,
     verify,
+    verify_batched,
+    verify_paged_tree,
     version,
     workspace_size,
 )

@@ -43,6 +43,9 @@ EXPORTED = (
     "tree_attn_prefix_pass",
     "tree_attn_suffix_merge",
     "tree_attn_verify_noalloc",
+    "tree_mask_build_batched",
+    "tree_attn_verify_batched",
+    "tree_attn_verify_paged_tree",
 )
 
 
@@ -87,6 +90,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_suffix_merge.restype = i32
     lib.tree_attn_verify_noalloc.argtypes = verify_args[:19] + [vp, vp]
     lib.tree_attn_verify_noalloc.restype = i32
+    lib.tree_mask_build_batched.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.tree_mask_build_batched.restype = i32
+    lib.tree_attn_verify_batched.argtypes = verify_args
+    lib.tree_attn_verify_batched.restype = i32
+    lib.tree_attn_verify_paged_tree.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, i32, i32,
+                                                i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
+    lib.tree_attn_verify_paged_tree.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -137,6 +147,23 @@ def mask_build(parents: torch.Tensor, mask_out: Optional[torch.Tensor] = None,
                                 _stream_handle(stream))
     if rc != 0:
         raise TreeAttnError("tree_mask_build", rc)
+    return mask_out
+
+
+def mask_build_batched(parents: torch.Tensor, mask_out: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Masks of a batch of trees: parents int32 [n][T] -> int64 [n][T] bits."""
+    _check(parents, "parents", (torch.int32,), 2)
+    n, T = parents.shape
+    if mask_out is None:
+        mask_out = torch.empty((n, T), dtype=torch.int64, device=parents.device)
+    _check(mask_out, "mask_out", _BITS64, 2)
+    if status is not None:
+        _check(status, "status", (torch.int32,))
+    rc = load().tree_mask_build_batched(_ptr(parents), T, n, _ptr(mask_out), _ptr(status),
+                                        _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_mask_build_batched", rc)
     return mask_out
 
 
@@ -200,6 +227,79 @@ def verify(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
         rc = lib.tree_attn_verify(*args)
     if rc != 0:
         raise TreeAttnError("tree_attn_verify", rc)
+    return out, lse
+
+
+def verify_batched(q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, masks, *,
+                   out=None, lse=None, workspace=None, status=None, softmax_scale=None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """tree_attn_verify with one tree per sequence (masks [B][T])."""
+    _check(masks, "masks", _BITS64, 2)
+    return _verify_generic("tree_attn_verify_batched", q, k_pages, v_pages, block_table,
+                           seq_lens, tree_k, tree_v, masks, out, lse, workspace, status,
+                           softmax_scale, stream)
+
+
+def verify_paged_tree(q, k_pages, v_pages, block_table, seq_lens, mask, *, out=None, lse=None,
+                      workspace=None, status=None, softmax_scale=None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split tree attention with the tree tokens' K/V inside the paged cache at
+    positions seq_lens[b] .. seq_lens[b] + T - 1; mask [T] or [B][T]."""
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 4)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(mask, "mask", _BITS64)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    mask_stride = T if mask.dim() == 2 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, d, T, 0, P)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = load().tree_attn_verify_paged_tree(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), _ptr(mask), mask_stride, _ptr(out), _ptr(lse), B, Hq, Hkv, d, T, P,
+        num_pages, float(softmax_scale), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_verify_paged_tree", rc)
+    return out, lse
+
+
+def _verify_generic(fn, q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, mask, out,
+                    lse, workspace, status, softmax_scale, stream):
+    bf = (torch.bfloat16,)
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (tree_k, "tree_k"),
+                 (tree_v, "tree_v")):
+        _check(t, n, bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, d, T, 0, P)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = getattr(load(), fn)(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), _ptr(tree_k), _ptr(tree_v), _ptr(mask), _ptr(out), _ptr(lse), B, Hq, Hkv,
+        d, T, P, num_pages, float(softmax_scale), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError(fn, rc)
     return out, lse
 
 

@@ -60,6 +60,9 @@ __device__ __forceinline__ int pick32(int lo, int hi, int node) {
 __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
                                                        uint64_t* __restrict__ mask,
                                                        int32_t* status) {
+    // CTA b builds the mask of tree b (a batch of trees is [B][T]).
+    parents += static_cast<size_t>(blockIdx.x) * T;
+    mask += static_cast<size_t>(blockIdx.x) * T;
     // The next kernel may start its prologue now; it waits for this grid
     // before reading anything this grid writes.
     ptx::grid_dep_launch();
@@ -745,6 +748,15 @@ struct MergeArgs {
     int B, Hq, Hkv, G, T, M, RB, P, max_pages, n_ctas;
     int wpr;  // warps per query row in the merge (1, 2, 4 or 8)
     float scale_log2;
+    int mask_stride;  // 0: one tree for the batch; T: tree b at mask[b * T]
+    // Tree tokens padded inside the paged cache (tree_k / tree_v unused):
+    // tree token j of sequence b sits at logical position seq_lens[b] + j.
+    int tree_in_cache;
+    const uint16_t* k_pages;
+    const uint16_t* v_pages;
+    const int32_t* block_table;
+    int num_pages;
+    int32_t* status;
 };
 
 template <int E>
@@ -861,8 +873,13 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     if (active && sub == 0) {
         float qv[E];
         load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
-        uint64_t bits = a.mask[t];
+        uint64_t bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
         if (a.T < 64) bits &= (1ull << a.T) - 1ull;
+        int L_b = 0;
+        if (a.tree_in_cache) {
+            bool bad_len;
+            L_b = clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad_len);
+        }
         while (bits != 0) {
             int js[4];
             int n = 0;
@@ -876,13 +893,43 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
                 }
             }
             float kv[4][E], vv[4][E];
+            if (a.tree_in_cache) {
+                // Position L_b + j of the paged cache (the tree padding).
+                int page[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i < n) {
+                for (int i = 0; i < 4; ++i) {
+                    page[i] = -1;
+                    const int pos = L_b + js[i];
+                    if (i < n && pos / a.P < a.max_pages)
+                        page[i] = a.block_table[static_cast<size_t>(b) * a.max_pages + pos / a.P];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i >= n) continue;
+                    const int pos = L_b + js[i];
+                    if (page[i] < 0 || page[i] >= a.num_pages) {
+                        if (lane == 0)
+                            report(a.status, pos / a.P < a.max_pages ? TREE_ATTN_STATUS_BAD_PAGE
+                                                                     : TREE_ATTN_STATUS_BAD_SEQ_LEN);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) kv[i][e] = vv[i][e] = 0.f;
+                        continue;
+                    }
                     const size_t off =
-                        ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
-                    load_bf16<E>(a.tree_k + off, kv[i]);
-                    load_bf16<E>(a.tree_v + off, vv[i]);
+                        ((static_cast<size_t>(page[i]) * a.Hkv + hk) * a.P + pos % a.P) * D +
+                        lane * E;
+                    load_bf16<E>(a.k_pages + off, kv[i]);
+                    load_bf16<E>(a.v_pages + off, vv[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < n) {
+                        const size_t off =
+                            ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
+                        load_bf16<E>(a.tree_k + off, kv[i]);
+                        load_bf16<E>(a.tree_v + off, vv[i]);
+                    }
                 }
             }
             float x[4];
@@ -1116,6 +1163,13 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.max_pages = v.max_pages;
     ma.n_ctas = v.n_ctas;
     ma.scale_log2 = v.scale_log2;
+    ma.mask_stride = v.mask_stride;
+    ma.tree_in_cache = v.tree_in_cache;
+    ma.k_pages = v.k_pages;
+    ma.v_pages = v.v_pages;
+    ma.block_table = v.block_table;
+    ma.num_pages = v.num_pages;
+    ma.status = v.status;
     // Warps per row from the expected partials per row: prefix CTAs per unit
     // (plus one for a straddled boundary) times the row copies.
     const long long units = static_cast<long long>(v.B) * v.Hkv * RB;
@@ -1132,9 +1186,10 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int32_t* status,
-                              cudaStream_t stream) {
-    return launch_pdl(tree_mask_kernel, dim3(1), dim3(32), 0, stream, parents, T, mask, status);
+cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64_t* mask,
+                              int32_t* status, cudaStream_t stream) {
+    return launch_pdl(tree_mask_kernel, dim3(n_trees), dim3(32), 0, stream, parents, T, mask,
+                      status);
 }
 
 cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,

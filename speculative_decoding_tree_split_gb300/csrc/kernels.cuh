@@ -24,11 +24,13 @@ struct VerifyArgs {
     int B, Hq, Hkv, d, T, P, max_pages, num_pages;
     int n_ctas;
     float scale_log2;
+    int mask_stride;    // 0: mask[T] shared by the batch; T: mask[B][T]
+    int tree_in_cache;  // tree K/V at positions seq_lens[b] .. +T of the paged cache
 };
 
-// Enqueue the mask builder (one warp).  Returns a cudaError_t.
-cudaError_t launch_mask_build(const int32_t* parents, int T, uint64_t* mask, int32_t* status,
-                              cudaStream_t stream);
+// Enqueue the mask builder (one warp per tree, n_trees trees of T nodes).
+cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64_t* mask,
+                              int32_t* status, cudaStream_t stream);
 
 // Enqueue the prefix pass (partials into a.ws).  `tmap_k`/`tmap_v` point at
 // encoded CUtensorMap objects (host memory, copied into the launch).

@@ -107,15 +107,22 @@ extern "C" {
 
 int tree_attn_version(void) { return 10000; }
 
+int tree_mask_build_batched(const int32_t* parents, int T, int n_trees, uint64_t* mask_out,
+                            int32_t* status, void* stream) {
+    if (T < 1 || T > TREE_ATTN_MAX_T || n_trees < 0) return TREE_ATTN_ERR_SHAPE;
+    if (n_trees == 0) return TREE_ATTN_OK;
+    if (parents == nullptr || mask_out == nullptr) return TREE_ATTN_ERR_NULL;
+    if (!aligned(parents, 4) || !aligned(mask_out, 8) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    const cudaError_t e = launch_mask_build(parents, T, n_trees, mask_out, status,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
 int tree_mask_build(const int32_t* parents, int T, uint64_t* mask_out, int32_t* status,
                     void* stream) {
     if (parents == nullptr || mask_out == nullptr) return TREE_ATTN_ERR_NULL;
-    if (T < 1 || T > TREE_ATTN_MAX_T) return TREE_ATTN_ERR_SHAPE;
-    if (!aligned(parents, 4) || !aligned(mask_out, 8) || !aligned(status, 4))
-        return TREE_ATTN_ERR_ALIGN;
-    const cudaError_t e =
-        launch_mask_build(parents, T, mask_out, status, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+    return tree_mask_build_batched(parents, T, 1, mask_out, status, stream);
 }
 
 size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T, int page_size,
@@ -211,13 +218,25 @@ int tree_attn_suffix_merge(const uint16_t* q, const int32_t* seq_lens, int max_p
                                                                            : TREE_ATTN_ERR_CUDA;
 }
 
-int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
-                          const int32_t* block_table, int max_pages_per_seq,
-                          const int32_t* seq_lens, const uint16_t* tree_k,
-                          const uint16_t* tree_v, const uint64_t* mask, uint16_t* out,
-                          float* lse, int B, int Hq, int Hkv, int d, int T, int page_size,
-                          int num_pages, float softmax_scale, void* workspace,
-                          size_t workspace_bytes, int32_t* status, void* stream, int n_ctas) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the verify entry points.  mask_stride: 0 (one tree) or T
+// (tree b at mask[b * T]); tree_in_cache: tree K/V live in the paged cache at
+// positions seq_lens[b] .. seq_lens[b] + T - 1 (tree_k / tree_v unused).
+int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                  const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                  const uint16_t* tree_k, const uint16_t* tree_v, const uint64_t* mask,
+                  int mask_stride, bool tree_in_cache, uint16_t* out, float* lse, int B, int Hq,
+                  int Hkv, int d, int T, int page_size, int num_pages, float softmax_scale,
+                  void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
+                  int n_ctas) {
+    if (mask_stride != 0 && mask_stride != T) return TREE_ATTN_ERR_SHAPE;
+    if (tree_in_cache) {
+        tree_k = k_pages;  // unused: keep the null checks below meaningful
+        tree_v = v_pages;
+    }
     int rc = check_common(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, softmax_scale);
     if (rc != TREE_ATTN_OK) return rc;
     if (num_pages < 1 || static_cast<long long>(num_pages) * Hkv * page_size >= (1LL << 31))
@@ -259,10 +278,55 @@ int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint
     a.num_pages = num_pages;
     a.n_ctas = n_ctas;
     a.scale_log2 = to_log2(softmax_scale);
+    a.mask_stride = mask_stride;
+    a.tree_in_cache = tree_in_cache ? 1 : 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = prefix_impl(a, k_pages, v_pages, st);
     if (rc != TREE_ATTN_OK) return rc;
     return launch_merge(a, st) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tree_attn_verify_ctas(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                          const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, const uint16_t* tree_k,
+                          const uint16_t* tree_v, const uint64_t* mask, uint16_t* out,
+                          float* lse, int B, int Hq, int Hkv, int d, int T, int page_size,
+                          int num_pages, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream, int n_ctas) {
+    return verify_common(q, k_pages, v_pages, block_table, max_pages_per_seq, seq_lens, tree_k,
+                         tree_v, mask, 0, false, out, lse, B, Hq, Hkv, d, T, page_size,
+                         num_pages, softmax_scale, workspace, workspace_bytes, status, stream,
+                         n_ctas);
+}
+
+int tree_attn_verify_batched(const uint16_t* q, const uint16_t* k_pages,
+                             const uint16_t* v_pages, const int32_t* block_table,
+                             int max_pages_per_seq, const int32_t* seq_lens,
+                             const uint16_t* tree_k, const uint16_t* tree_v,
+                             const uint64_t* masks, uint16_t* out, float* lse, int B, int Hq,
+                             int Hkv, int d, int T, int page_size, int num_pages,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             int32_t* status, void* stream) {
+    return verify_common(q, k_pages, v_pages, block_table, max_pages_per_seq, seq_lens, tree_k,
+                         tree_v, masks, T, false, out, lse, B, Hq, Hkv, d, T, page_size,
+                         num_pages, softmax_scale, workspace, workspace_bytes, status, stream, 0);
+}
+
+int tree_attn_verify_paged_tree(const uint16_t* q, const uint16_t* k_pages,
+                                const uint16_t* v_pages, const int32_t* block_table,
+                                int max_pages_per_seq, const int32_t* seq_lens,
+                                const uint64_t* mask, int mask_stride, uint16_t* out, float* lse,
+                                int B, int Hq, int Hkv, int d, int T, int page_size,
+                                int num_pages, float softmax_scale, void* workspace,
+                                size_t workspace_bytes, int32_t* status, void* stream) {
+    return verify_common(q, k_pages, v_pages, block_table, max_pages_per_seq, seq_lens, nullptr,
+                         nullptr, mask, mask_stride, true, out, lse, B, Hq, Hkv, d, T,
+                         page_size, num_pages, softmax_scale, workspace, workspace_bytes, status,
+                         stream, 0);
 }
 
 int tree_attn_verify(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,

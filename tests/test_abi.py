@@ -119,3 +119,38 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         ta.mask_build(torch.tensor([-1, 0], dtype=torch.int32))
+
+
+def _paged_tree(lib, mask_stride=0, **kw):
+    args = dict(q=A16, k=A16, v=A16, bt=A16, maxp=4, sl=A16, mask=A16, out=A16, lse=A16, B=2,
+                Hq=8, Hkv=2, d=128, T=4, P=64, num_pages=8, scale=0.1)
+    args.update(kw)
+    return lib.tree_attn_verify_paged_tree(
+        args["q"], args["k"], args["v"], args["bt"], args["maxp"], args["sl"], args["mask"],
+        mask_stride, args["out"], args["lse"], args["B"], args["Hq"], args["Hkv"], args["d"],
+        args["T"], args["P"], args["num_pages"], args["scale"], A16, 1 << 30, None, None)
+
+
+def test_paged_tree_host_checks(lib):
+    # mask stride must be 0 (one tree) or T (one tree per sequence)
+    for stride in (1, 3, 5, -4):
+        assert _paged_tree(lib, mask_stride=stride) == -2
+    assert _paged_tree(lib, mask_stride=4, d=96) == -2
+    for name in ("q", "k", "v", "bt", "sl", "mask", "out", "lse"):
+        assert _paged_tree(lib, **{name: None}) == -1
+    assert _paged_tree(lib, k=A16 + 2) == -3
+    assert _paged_tree(lib, B=0, q=None) == 0
+
+
+def test_batched_entry_host_checks(lib):
+    a = A16
+    verify = lib.tree_attn_verify_batched
+    base = [a, a, a, a, 4, a, a, a, a, a, a, 2, 8, 2, 128, 4, 64, 8, 0.1, a, 1 << 30, None, None]
+    assert verify(*base[:8], None, *base[9:]) == -1       # masks
+    bad_t = list(base)
+    bad_t[15] = 65
+    assert verify(*bad_t) == -2
+    assert lib.tree_mask_build_batched(a, 4, -1, a, None, None) == -2
+    assert lib.tree_mask_build_batched(None, 4, 2, a, None, None) == -1
+    assert lib.tree_mask_build_batched(a, 4, 2, a + 4, None, None) == -3
+    assert lib.tree_mask_build_batched(a, 4, 0, a, None, None) == 0

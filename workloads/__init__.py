@@ -26,6 +26,15 @@ Recipe (all draws come from one ``torch.Generator('cpu')`` seeded per config):
    table slots hold -1.
 4. ``q``, ``k_pages``, ``v_pages``, ``tree_k``, ``tree_v``: i.i.d. N(0, 1) in
    fp32, rounded to bf16 (round to nearest even, torch's conversion).
+
+Two layout variants (both off by default, so the default draws are unchanged):
+
+* ``per_sequence_trees``: step 2 runs once per sequence, giving ``parents``
+  of shape [B][T] (one draft tree per sequence).
+* ``tree_in_cache``: the tree tokens live in the paged cache ("paged KV with
+  tree padding"): each sequence's pages cover ``L_b + T`` positions and token
+  ``j``'s K/V (the same ``tree_k`` / ``tree_v`` draws) is written at logical
+  position ``L_b + j``.
 """
 from __future__ import annotations
 
@@ -134,7 +143,7 @@ class Workload:
     """All inputs of one ``tree_attn_verify`` call, as CPU tensors."""
 
     cfg: Config
-    parents: torch.Tensor        # int32 [T]
+    parents: torch.Tensor        # int32 [T], or [B][T] with per-sequence trees
     seq_lens: torch.Tensor       # int32 [B]
     block_table: torch.Tensor    # int32 [B][max_pages_per_seq]
     q: torch.Tensor              # bf16 [B][T][Hq][d]
@@ -143,6 +152,18 @@ class Workload:
     tree_k: torch.Tensor         # bf16 [B][T][Hkv][d]
     tree_v: torch.Tensor         # bf16 [B][T][Hkv][d]
     scale: float
+    tree_in_cache: bool = False  # tree K/V also written at positions L_b + j
+
+    def sequence(self, b: int) -> "Workload":
+        """Sequence ``b`` alone, as a B = 1 workload with its own tree (the
+        pages are shared; the block table row is kept)."""
+        c = dataclasses.replace(self.cfg, B=1)
+        par = self.parents[b] if self.parents.dim() == 2 else self.parents
+        return Workload(cfg=c, parents=par.clone(), seq_lens=self.seq_lens[b:b + 1].clone(),
+                        block_table=self.block_table[b:b + 1].clone(), q=self.q[b:b + 1],
+                        k_pages=self.k_pages, v_pages=self.v_pages,
+                        tree_k=self.tree_k[b:b + 1], tree_v=self.tree_v[b:b + 1],
+                        scale=self.scale, tree_in_cache=self.tree_in_cache)
 
     @property
     def num_pages(self) -> int:
@@ -174,12 +195,15 @@ def make_workload(cfg: Config, seed: Optional[int] = None, *,
                   parents: Optional[torch.Tensor] = None,
                   max_pages_per_seq: Optional[int] = None,
                   extra_pages: int = 0,
-                  q_zero: bool = False) -> Workload:
+                  q_zero: bool = False,
+                  per_sequence_trees: bool = False,
+                  tree_in_cache: bool = False) -> Workload:
     """Build the seeded inputs of ``cfg`` (recipe in the module docstring).
 
     ``seq_lens`` / ``parents`` override the drawn values (edge-case tests);
     ``max_pages_per_seq`` widens the block table; ``extra_pages`` adds unused
-    physical pages; ``q_zero`` zeroes the queries (closed-form tests).
+    physical pages; ``q_zero`` zeroes the queries (closed-form tests);
+    ``per_sequence_trees`` / ``tree_in_cache`` select the layout variants.
     """
     gen = torch.Generator("cpu")
     gen.manual_seed(cfg.seed if seed is None else seed)
@@ -196,15 +220,20 @@ def make_workload(cfg: Config, seed: Optional[int] = None, *,
         sl = torch.tensor(seq_lens, dtype=torch.int64)
     seq_lens_t = sl.to(torch.int32)
 
-    if parents is None:
+    def draw_tree() -> torch.Tensor:
         if cfg.tree == "chain":
-            parents_t = chain_tree(cfg.T)
-        else:
-            parents_t = random_tree(cfg.T, cfg.max_depth, cfg.max_branch, gen)
-    else:
-        parents_t = parents.to(torch.int32).clone()
+            return chain_tree(cfg.T)
+        return random_tree(cfg.T, cfg.max_depth, cfg.max_branch, gen)
 
-    pages_per = [(int(x) + P - 1) // P for x in sl.tolist()]
+    if parents is not None:
+        parents_t = parents.to(torch.int32).clone()
+    elif per_sequence_trees:
+        parents_t = torch.stack([draw_tree() for _ in range(B)])
+    else:
+        parents_t = draw_tree()
+
+    span = cfg.T if tree_in_cache else 0
+    pages_per = [(int(x) + span + P - 1) // P for x in sl.tolist()]
     used_pages = sum(pages_per)
     num_pages = used_pages + extra_pages
     width = max(pages_per + [1])
@@ -228,6 +257,13 @@ def make_workload(cfg: Config, seed: Optional[int] = None, *,
     v_pages = _randn_bf16((num_pages, Hkv, P, d), gen)
     tree_k = _randn_bf16((B, T, Hkv, d), gen)
     tree_v = _randn_bf16((B, T, Hkv, d), gen)
+    if tree_in_cache:
+        for b in range(B):
+            for j in range(T):
+                pos = int(sl[b]) + j
+                page = int(bt[b, pos // P])
+                k_pages[page, :, pos % P] = tree_k[b, j]
+                v_pages[page, :, pos % P] = tree_v[b, j]
     return Workload(cfg=cfg, parents=parents_t, seq_lens=seq_lens_t, block_table=bt,
                     q=q, k_pages=k_pages, v_pages=v_pages, tree_k=tree_k, tree_v=tree_v,
-                    scale=1.0 / math.sqrt(d))
+                    scale=1.0 / math.sqrt(d), tree_in_cache=tree_in_cache)
