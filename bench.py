@@ -58,6 +58,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", choices=sorted(CONFIGS), default="llama8b")
+    p.add_argument("--layout", choices=["shared", "per_seq", "paged_tree"], default="shared",
+                   help="shared: one draft tree for the batch, tree K/V in their own buffers; "
+                        "per_seq: one tree per sequence; paged_tree: tree K/V padded into the "
+                        "paged cache at positions L_b + j")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="bound on the CPU-baseline sample (oracle wall time)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -95,8 +99,13 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def workload_desc(cfg):
-    return cfg.describe()
+def workload_desc(cfg, layout="shared"):
+    return cfg.describe() + ("" if layout == "shared" else f" layout={layout}")
+
+
+def make_layout_workload(cfg, layout, seed=None):
+    return make_workload(cfg, seed=seed, per_sequence_trees=(layout == "per_seq"),
+                         tree_in_cache=(layout == "paged_tree"))
 
 
 def algorithmic_bytes(wl):
@@ -193,21 +202,40 @@ def emit(obj):
 # ---------------------------------------------------------------------------
 # CPU side: the fp64 oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_tokens_per_s(wl, budget_s, max_tokens=None):
-    """Time the oracle on whole tree tokens (all Hq heads of one (b, i)),
-    round-robin over the batch, until `budget_s` of wall time is spent."""
+def oracle_token_fn(wl):
+    """f(b, i): the oracle on one tree token (all Hq query heads of sequence b,
+    node i), with sequence b's own tree mask."""
     import oracle
     orc = oracle.get()
     c = wl.cfg
-    mask = orc.tree_mask(wl.parents.tolist())
     threads = len(os.sched_getaffinity(0))
+    if wl.parents.dim() == 2:
+        seqs = [wl.sequence(b) for b in range(c.B)]
+        masks = [orc.tree_mask(s.parents.tolist()) for s in seqs]
+    else:
+        seqs, masks = None, orc.tree_mask(wl.parents.tolist())
+
+    def f(b, i):
+        if seqs is None:
+            rows = np.array([(b, i, h) for h in range(c.Hq)], dtype=np.int32)
+            orc.verify_rows(wl, masks, rows, threads=threads)
+        else:
+            rows = np.array([(0, i, h) for h in range(c.Hq)], dtype=np.int32)
+            orc.verify_rows(seqs[b], masks[b], rows, threads=threads)
+
+    return f, threads
+
+
+def oracle_tokens_per_s(wl, budget_s, max_tokens=None):
+    """Time the oracle on whole tree tokens (all Hq heads of one (b, i)),
+    round-robin over the batch, until `budget_s` of wall time is spent."""
+    c = wl.cfg
+    f, threads = oracle_token_fn(wl)
     tokens = [(b, i) for b in range(c.B) for i in range(c.T)]
     done = 0
     t0 = time.perf_counter()
     while True:
-        b, i = tokens[done % len(tokens)]
-        rows = np.array([(b, i, h) for h in range(c.Hq)], dtype=np.int32)
-        orc.verify_rows(wl, mask, rows, threads=threads)
+        f(*tokens[done % len(tokens)])
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_tokens is not None and done >= max_tokens):
@@ -220,17 +248,12 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = CONFIGS[args.config]
-    wl = make_workload(cfg)
-    import oracle
-    orc = oracle.get()
-    mask = orc.tree_mask(wl.parents.tolist())
-    threads = len(os.sched_getaffinity(0))
+    wl = make_layout_workload(cfg, args.layout)
+    f, threads = oracle_token_fn(wl)
     tokens = [(b, i) for b in range(cfg.B) for i in range(cfg.T)]
 
     def step(n):
-        b, i = tokens[n % len(tokens)]
-        rows = np.array([(b, i, h) for h in range(cfg.Hq)], dtype=np.int32)
-        orc.verify_rows(wl, mask, rows, threads=threads)
+        f(*tokens[n % len(tokens)])
 
     for n in range(args.warmup):
         step(n)
@@ -243,7 +266,7 @@ def run_reference(args):
           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": workload_desc(cfg)},
+          "config": {"workload": workload_desc(cfg, args.layout)},
           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                            "sample": f"each step = one tree token (all {cfg.Hq} query heads of "
                                      f"one (sequence, node)) of the workload, round-robin"},
@@ -267,7 +290,8 @@ def run_ours(args):
     ta.load()
 
     cfg = CONFIGS[args.config]
-    wl = make_workload(cfg, seed=cfg.seed + rank)
+    layout = args.layout
+    wl = make_layout_workload(cfg, layout, seed=cfg.seed + rank)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 132 * 1024 * 1024
     kv_alloc = wl.k_pages.numel() * 2 * 2
@@ -282,17 +306,30 @@ def run_ours(args):
     tv = wl.tree_v.to(dev)
     kps = [wl.k_pages.to(dev) for _ in range(R)]
     vps = [wl.v_pages.to(dev) for _ in range(R)]
-    mask = torch.empty(cfg.T, dtype=torch.int64, device=dev)
+    mask = torch.empty(tuple(wl.parents.shape), dtype=torch.int64, device=dev)
     out = torch.empty_like(q)
     lse = torch.empty(cfg.B, cfg.T, cfg.Hq, dtype=torch.float32, device=dev)
     ws_bytes = ta.workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.T, 0, cfg.page)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    def hot_path(par, q_, k_, v_, bt_, sl_, tk_, tv_):
+        """One pass of the whole path: masks, then split tree attention."""
+        if layout == "per_seq":
+            ta.mask_build_batched(par, mask_out=mask, status=status)
+            ta.verify_batched(q_, k_, v_, bt_, sl_, tk_, tv_, mask, out=out, lse=lse,
+                              workspace=ws, status=status, softmax_scale=wl.scale)
+        elif layout == "paged_tree":
+            ta.mask_build(par, mask_out=mask, status=status)
+            ta.verify_paged_tree(q_, k_, v_, bt_, sl_, mask, out=out, lse=lse, workspace=ws,
+                                 status=status, softmax_scale=wl.scale)
+        else:
+            ta.mask_build(par, mask_out=mask, status=status)
+            ta.verify(q_, k_, v_, bt_, sl_, tk_, tv_, mask, out=out, lse=lse, workspace=ws,
+                      status=status, softmax_scale=wl.scale)
+
     def step(r):
-        ta.mask_build(parents, mask_out=mask, status=status)
-        ta.verify(q, kps[r % R], vps[r % R], bt, sl, tk, tv, mask, out=out, lse=lse,
-                  workspace=ws, status=status, softmax_scale=wl.scale)
+        hot_path(parents, q, kps[r % R], vps[r % R], bt, sl, tk, tv)
 
     def prefix_only(r):
         ta.prefix_pass(q, kps[r % R], vps[r % R], bt, sl, ws, status=status,
@@ -364,7 +401,7 @@ def run_ours(args):
     achieved = nbytes["prefix_kernel"] / (ms_prefix * 1e-3) / 1e9
     sha = kernel_source_sha()
     traffic = None
-    rec = NCU_TRAFFIC.get(args.config)
+    rec = NCU_TRAFFIC.get(args.config) if layout == "shared" else None
     if rec is not None and rec[0] == sha:
         traffic = rec[1]
 
@@ -372,10 +409,12 @@ def run_ours(args):
     # step, out/lse -> pinned host, every step
     e2e = None
     if not args.no_e2e:
-        h = {k: v.pin_memory() for k, v in dict(
-            parents=wl.parents, q=wl.q, k=wl.k_pages, v=wl.v_pages, bt=wl.block_table,
-            sl=wl.seq_lens, tk=wl.tree_k, tv=wl.tree_v).items()}
+        host = dict(parents=wl.parents, q=wl.q, k=wl.k_pages, v=wl.v_pages, bt=wl.block_table,
+                    sl=wl.seq_lens, tk=wl.tree_k, tv=wl.tree_v)
         d = dict(parents=parents, q=q, k=kps[0], v=vps[0], bt=bt, sl=sl, tk=tk, tv=tv)
+        if layout == "paged_tree":   # the tree K/V travel inside the pages
+            del host["tk"], host["tv"]
+        h = {k: v.pin_memory() for k, v in host.items()}
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in h.values())
@@ -385,9 +424,7 @@ def run_ours(args):
         def e2e_step():
             for key in h:
                 d[key].copy_(h[key], non_blocking=True)
-            ta.mask_build(d["parents"], mask_out=mask, status=status)
-            ta.verify(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["tk"], d["tv"], mask, out=out,
-                      lse=lse, workspace=ws, status=status, softmax_scale=wl.scale)
+            hot_path(d["parents"], d["q"], d["k"], d["v"], d["bt"], d["sl"], d["tk"], d["tv"])
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -419,7 +456,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg), "tokens_per_step_per_gpu": cfg.B * cfg.T,
+            "config": {"workload": workload_desc(cfg, layout), "tokens_per_step_per_gpu": cfg.B * cfg.T,
                        "l2": f"{R} rotating device copies of the KV cache "
                              f"({R * kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)",
                        "parallelism": f"replicas x{world}", "timing": "one CUDA graph of the "
