@@ -62,6 +62,10 @@ def parse_args():
                    help="shared: one draft tree for the batch, tree K/V in their own buffers; "
                         "per_seq: one tree per sequence; paged_tree: tree K/V padded into the "
                         "paged cache at positions L_b + j")
+    p.add_argument("--path", choices=["verify", "accept_commit"], default="verify",
+                   help="verify: the split tree attention step (default); accept_commit: "
+                        "greedy acceptance of the verified tree plus the KV commit of the "
+                        "accepted path (tree tokens in the paged cache)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="bound on the CPU-baseline sample (oracle wall time)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -477,9 +481,207 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# the step after verification: greedy acceptance + KV commit
+# ---------------------------------------------------------------------------
+ACCEPT_METRIC = "committed sequences/s per layer"
+ACCEPT_UNIT = "sequences/s"
+
+
+def accept_inputs(cfg, seed):
+    """Per-sequence trees with the tree tokens in the paged cache, plus draft
+    and target tokens from a 2-token alphabet (about half the edges match, so
+    paths of several nodes are common)."""
+    wl = make_workload(cfg, seed=seed, per_sequence_trees=True, tree_in_cache=True)
+    g = torch.Generator().manual_seed(1000 + seed)
+    draft = torch.randint(0, 2, (cfg.B, cfg.T), generator=g, dtype=torch.int32)
+    target = torch.randint(0, 2, (cfg.B, cfg.T), generator=g, dtype=torch.int32)
+    return wl, draft, target
+
+
+def oracle_accept_commit_per_s(wl, draft, target, budget_s, steps=None):
+    """Time the acceptance / commit oracle on the whole batch, step after step."""
+    from workloads import bf16_bits
+    import oracle.accept as acc
+    k = bf16_bits(wl.k_pages)
+    v = bf16_bits(wl.v_pages)
+    bt = wl.block_table.numpy()
+    sl = wl.seq_lens.numpy()
+    par, dr, tg = wl.parents.numpy(), draft.numpy(), target.numpy()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        n, path, _ = acc.greedy_accept_batch(par, dr, tg)
+        acc.kv_commit(k, v, bt, sl, None, None, path, n, wl.cfg.page)
+        done += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and done >= steps) or (steps is None and el >= budget_s):
+            break
+    return done * wl.cfg.B / el, done, el
+
+
+def run_accept_commit(args):
+    import speculative_decoding_tree_split_gb300 as ta
+
+    world, rank, local = dist_info()
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl, draft, target = accept_inputs(cfg, cfg.seed)
+        oracle_accept_commit_per_s(wl, draft, target, 0, steps=max(args.warmup, 1))
+        v, n_steps, el = oracle_accept_commit_per_s(wl, draft, target, 0, steps=args.steps)
+        emit({"impl": "reference", "metric": ACCEPT_METRIC, "value": v, "unit": ACCEPT_UNIT,
+              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+              "ms_per_step": 1e3 * el / n_steps, "higher_is_better": True, "scaling": "weak",
+              "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+              "config": {"workload": workload_desc(cfg, "paged_tree") + " path=accept_commit"},
+              "cpu_baseline": {"value": v, "unit": ACCEPT_UNIT, "cores": 1, "kind": "oracle",
+                               "sample": f"{n_steps} whole steps"},
+              "e2e": {"value": v, "unit": ACCEPT_UNIT, "h2d_bytes_per_step": 0,
+                      "d2h_bytes_per_step": 0}})
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta.build()
+    ta.load()
+    wl, draft, target = accept_inputs(cfg, cfg.seed + rank)
+    parents = wl.parents.to(dev)
+    d_draft, d_target = draft.to(dev), target.to(dev)
+    k, v = wl.k_pages.to(dev), wl.v_pages.to(dev)
+    bt, sl = wl.block_table.to(dev), wl.seq_lens.to(dev)
+    B, T = cfg.B, cfg.T
+    masks = torch.empty((B, T), dtype=torch.int64, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, T), dtype=torch.int32, device=dev)
+    bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    sl_out = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ta.mask_build_batched(parents, mask_out=masks, status=status)
+
+    def accept_only(_r=0):
+        ta.greedy_accept(masks, d_draft, d_target, accept_len=n, accept_path=path,
+                         bonus_token=bonus)
+
+    def commit_only(_r=0):
+        ta.kv_commit(k, v, bt, sl, path, n, seq_lens_out=sl_out, status=status)
+
+    def step(_r=0):
+        accept_only()
+        commit_only()
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(max(args.warmup, 1)):
+            step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    K = args.steps
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(K):
+                fn()
+        return g
+
+    def timed(g):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_.record()
+        g.replay()
+        e_.record()
+        torch.cuda.synchronize()
+        return s_.elapsed_time(e_) / K
+
+    g_step, g_acc, g_com = graph_of(step), graph_of(accept_only), graph_of(commit_only)
+    g_step.replay()
+    sampler = ClockSampler(smi_gpu_id(torch.cuda.get_device_properties(dev), local))
+    if not args.no_clocks:
+        sampler.start()
+        t_end = time.perf_counter() + 1.2
+        while time.perf_counter() < t_end:
+            g_step.replay()
+            torch.cuda.synchronize()
+    ms_step = timed(g_step)
+    ms_acc = timed(g_acc)
+    ms_com = timed(g_com)
+    clocks = sampler.stop() if not args.no_clocks else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    ms_step, ms_acc, ms_com = max_over_ranks([ms_step, ms_acc, ms_com], dev)
+    n_h = n.cpu()
+    rows = int(n_h.sum().item())
+    commit_bytes = rows * cfg.Hkv * cfg.d * 2 * 2 * 2   # K and V rows, read + write
+    peak, peak_src = measured_hbm_peak()
+    achieved = commit_bytes / (ms_com * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        h_draft, h_target = draft.pin_memory(), target.pin_memory()
+        h_n = torch.empty(B, dtype=torch.int32).pin_memory()
+        h_bonus = torch.empty(B, dtype=torch.int32).pin_memory()
+        h2d = 2 * B * T * 4
+        d2h = 2 * B * 4
+
+        def e2e_step():
+            d_draft.copy_(h_draft, non_blocking=True)
+            d_target.copy_(h_target, non_blocking=True)
+            step()
+            h_n.copy_(n, non_blocking=True)
+            h_bonus.copy_(bonus, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        for _ in range(K):
+            e2e_step()
+        e_.record()
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks([s_.elapsed_time(e_) / K], dev)[0]
+        e2e = {"value": B * world / (ms_e2e * 1e-3), "unit": ACCEPT_UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        vcpu, n_steps, el = oracle_accept_commit_per_s(wl, draft, target, args.cpu_seconds)
+        cpu = {"value": vcpu, "unit": ACCEPT_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_steps} whole steps ({el:.1f} s)"}
+    if rank == 0:
+        emit({
+            "metric": ACCEPT_METRIC, "value": B * world / (ms_step * 1e-3), "unit": ACCEPT_UNIT,
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(cfg, "paged_tree") + " path=accept_commit",
+                       "l2": "inputs are a few KB and stay in L2 (latency-bound step)",
+                       "accepted_rows_per_step": rows,
+                       "timing": "one CUDA graph of the K steps, CUDA events"},
+            "accept_kernel_us": ms_acc * 1e3, "commit_kernel_us": ms_com * 1e3,
+            "roofline": {"bound": "hbm", "kernel": "kv_commit_kernel", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "algorithmic_bytes_per_launch": commit_bytes,
+                         "peak_source": peak_src,
+                         "note": "latency-bound: a few KB per launch"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * K, "cpu_baseline": cpu,
+        })
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.path == "accept_commit":
+        run_accept_commit(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

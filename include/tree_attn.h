@@ -57,6 +57,8 @@ extern "C" {
 #define TREE_ATTN_STATUS_BAD_PAGE 2     /* block_table entry outside [0, num_pages)   */
 #define TREE_ATTN_STATUS_BAD_SEQ_LEN 3  /* seq_lens[b] < 0 or > max_pages_per_seq*P   */
 #define TREE_ATTN_STATUS_TIMEOUT 4      /* an internal pipeline wait gave up           */
+#define TREE_ATTN_STATUS_BAD_PATH 5     /* accept_len outside [0, T] or a path node     */
+                                        /* outside [0, T) (tree_kv_commit)              */
 
 /* Limits. */
 #define TREE_ATTN_MAX_T 64
@@ -206,6 +208,62 @@ TREE_ATTN_API int tree_attn_verify_paged_tree(const uint16_t *q, const uint16_t 
                                               int page_size, int num_pages, float softmax_scale,
                                               void *workspace, size_t workspace_bytes,
                                               int32_t *status, void *stream);
+
+/*
+ * tree_greedy_accept -- greedy acceptance of the verified draft tree
+ * ("Efficient Speculative Decoding for Llama at Scale", fdeinterviews.com
+ * summary, opening paragraph: the service commits one accepted path; greedy
+ * drafting and verification per the mlsanity.com referee report, Summary).
+ *
+ *   mask           uint64 [T] (mask_stride 0, one tree) or [B][T] (mask_stride
+ *                  T): ancestor-or-self bits as tree_mask_build writes them
+ *   draft_tokens   int32 [B][T]: token of tree node i
+ *   target_tokens  int32 [B][T]: the target's greedy (argmax) token after
+ *                  node i, i.e. its prediction for node i's children
+ *   accept_len     int32 [B] out: nodes on the committed path (root included)
+ *   accept_path    int32 [B][T] out: the path's nodes root first, then -1
+ *   bonus_token    int32 [B] out: target_tokens at the path's last node
+ *
+ * A root is accepted; node i is accepted when its parent is and
+ * draft_tokens[i] == target_tokens[parent].  The path ends at the deepest
+ * accepted node, the lowest index among equally deep ones.  Integer work:
+ * results are exact.  All pointers device memory owned by the caller; async
+ * on `stream`.  Returns 0, -1 (NULL), -2 (T outside [1, 64], B < 0, stride
+ * neither 0 nor T), -3 (misaligned), -5 (launch failed).
+ */
+TREE_ATTN_API int tree_greedy_accept(const uint64_t *mask, int mask_stride,
+                                     const int32_t *draft_tokens, const int32_t *target_tokens,
+                                     int B, int T, int32_t *accept_len, int32_t *accept_path,
+                                     int32_t *bonus_token, void *stream);
+
+/*
+ * tree_kv_commit -- write the accepted path's K/V into the paged cache so
+ * that it holds the committed history only (fdeinterviews.com summary,
+ * paragraph on hidden correctness obligations; mlsanity.com referee report,
+ * minor comment on Section 3.3).  For sequence b, path node accept_path[b][k]
+ * (k < accept_len[b]) goes to logical position seq_lens[b] + k.
+ *
+ *   tree_k, tree_v  bf16 [B][T][Hkv][d] sources, or both NULL when the tree
+ *                   tokens already sit in the cache at seq_lens[b] + j
+ *                   (tree_attn_verify_paged_tree layout); that compaction is
+ *                   done in place, every row read before any is written
+ *   seq_lens_out    nullable int32 [B]: seq_lens[b] + accept_len[b]; must not
+ *                   be seq_lens itself (-2)
+ *   status          nullable: TREE_ATTN_STATUS_BAD_PATH, _BAD_PAGE (a target
+ *                   position's page outside [0, num_pages)), _BAD_SEQ_LEN (a
+ *                   position past max_pages_per_seq * page_size); rows that
+ *                   fail are skipped
+ *
+ * The pages that positions [seq_lens[b], seq_lens[b] + T) map to must be
+ * mapped by the caller and not shared with another sequence of the batch.
+ * Shapes as tree_attn_verify.  Returns 0, -1, -2, -3, -5.
+ */
+TREE_ATTN_API int tree_kv_commit(uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
+                                 int max_pages_per_seq, const int32_t *seq_lens,
+                                 const uint16_t *tree_k, const uint16_t *tree_v,
+                                 const int32_t *accept_path, const int32_t *accept_len,
+                                 int32_t *seq_lens_out, int B, int Hkv, int d, int T,
+                                 int page_size, int num_pages, int32_t *status, void *stream);
 
 /*
  * tree_attn_prefix_pass / tree_attn_suffix_merge -- the two passes of

@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     STATUS_BAD_PARENT,
     STATUS_BAD_SEQ_LEN,
     STATUS_TIMEOUT,
+    STATUS_BAD_PATH,
     TreeAttnError,
     load,
     mask_build,
@@ -27,6 +28,8 @@ from ._lib import (  # noqa: F401
     verify,
     verify_batched,
     verify_paged_tree,
+    greedy_accept,
+    kv_commit,
     version,
     workspace_size,
 )

@@ -31,6 +31,7 @@ STATUS_BAD_PARENT = 1
 STATUS_BAD_PAGE = 2
 STATUS_BAD_SEQ_LEN = 3
 STATUS_TIMEOUT = 4
+STATUS_BAD_PATH = 5
 MAX_T = 64
 
 EXPORTED = (
@@ -46,6 +47,8 @@ EXPORTED = (
     "tree_mask_build_batched",
     "tree_attn_verify_batched",
     "tree_attn_verify_paged_tree",
+    "tree_greedy_accept",
+    "tree_kv_commit",
 )
 
 
@@ -97,6 +100,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_verify_paged_tree.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, i32, i32,
                                                 i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     lib.tree_attn_verify_paged_tree.restype = i32
+    lib.tree_greedy_accept.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]
+    lib.tree_greedy_accept.restype = i32
+    lib.tree_kv_commit.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                   i32, i32, vp, vp]
+    lib.tree_kv_commit.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -301,6 +309,60 @@ def _verify_generic(fn, q, k_pages, v_pages, block_table, seq_lens, tree_k, tree
     if rc != 0:
         raise TreeAttnError(fn, rc)
     return out, lse
+
+
+def greedy_accept(mask, draft_tokens, target_tokens, *, accept_len=None, accept_path=None,
+                  bonus_token=None, stream=None):
+    """Greedy acceptance: mask int64 [T] or [B][T]; draft / target int32 [B][T].
+    Returns (accept_len [B], accept_path [B][T], bonus_token [B]), int32."""
+    _check(mask, "mask", _BITS64)
+    _check(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    _check(target_tokens, "target_tokens", (torch.int32,), 2)
+    B, T = draft_tokens.shape
+    if tuple(target_tokens.shape) != (B, T) or mask.shape[-1] != T:
+        raise ValueError("draft_tokens, target_tokens and mask disagree on B or T")
+    dev = draft_tokens.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if accept_path is None:
+        accept_path = torch.empty((B, T), dtype=torch.int32, device=dev)
+    if bonus_token is None:
+        bonus_token = torch.empty(B, dtype=torch.int32, device=dev)
+    stride = T if mask.dim() == 2 else 0
+    rc = load().tree_greedy_accept(_ptr(mask), stride, _ptr(draft_tokens), _ptr(target_tokens),
+                                   B, T, _ptr(accept_len), _ptr(accept_path), _ptr(bonus_token),
+                                   _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_greedy_accept", rc)
+    return accept_len, accept_path, bonus_token
+
+
+def kv_commit(k_pages, v_pages, block_table, seq_lens, accept_path, accept_len, *,
+              tree_k=None, tree_v=None, seq_lens_out=None, status=None, stream=None):
+    """Write each sequence's accepted path K/V at positions seq_lens[b] + k
+    (in place in k_pages / v_pages).  tree_k / tree_v None: the tree tokens
+    are in the cache already.  Returns seq_lens_out (seq_lens + accept_len)."""
+    bf = (torch.bfloat16,)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(accept_path, "accept_path", (torch.int32,), 2)
+    _check(accept_len, "accept_len", (torch.int32,), 1)
+    if tree_k is not None:
+        _check(tree_k, "tree_k", bf, 4)
+        _check(tree_v, "tree_v", bf, 4)
+    num_pages, Hkv, P, d = k_pages.shape
+    B, T = accept_path.shape
+    if seq_lens_out is None:
+        seq_lens_out = torch.empty(B, dtype=torch.int32, device=seq_lens.device)
+    rc = load().tree_kv_commit(_ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                               block_table.shape[1], _ptr(seq_lens), _ptr(tree_k), _ptr(tree_v),
+                               _ptr(accept_path), _ptr(accept_len), _ptr(seq_lens_out), B, Hkv,
+                               d, T, P, num_pages, _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_kv_commit", rc)
+    return seq_lens_out
 
 
 def prefix_pass(q, k_pages, v_pages, block_table, seq_lens, workspace, *, T=None,

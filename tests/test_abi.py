@@ -154,3 +154,41 @@ def test_batched_entry_host_checks(lib):
     assert lib.tree_mask_build_batched(None, 4, 2, a, None, None) == -1
     assert lib.tree_mask_build_batched(a, 4, 2, a + 4, None, None) == -3
     assert lib.tree_mask_build_batched(a, 4, 0, a, None, None) == 0
+
+
+def test_greedy_accept_host_checks(lib):
+    a = A16
+    f = lib.tree_greedy_accept
+    assert f(a, 0, a, a, 2, 0, a, a, a, None) == -2          # T = 0
+    assert f(a, 0, a, a, 2, 65, a, a, a, None) == -2         # T > 64
+    assert f(a, 3, a, a, 2, 4, a, a, a, None) == -2          # stride neither 0 nor T
+    assert f(a, 0, a, a, -1, 4, a, a, a, None) == -2
+    assert f(a, 0, a, a, 0, 4, None, None, None, None) == 0  # empty batch
+    for k in range(6):
+        args = [a, 0, a, a, 2, 4, a, a, a, None]
+        args[[0, 2, 3, 6, 7, 8][k]] = None
+        assert f(*args) == -1
+    assert f(a + 4, 0, a, a, 2, 4, a, a, a, None) == -3
+    assert f(a, 0, a + 2, a, 2, 4, a, a, a, None) == -3
+
+
+def _commit(lib, **kw):
+    args = dict(k=A16, v=A16, bt=A16, maxp=4, sl=A16, tk=A16, tv=A16, path=A16, n=A16,
+                sl_out=A16 + 256, B=2, Hkv=2, d=128, T=4, P=64, num_pages=8, status=None)
+    args.update(kw)
+    return lib.tree_kv_commit(args["k"], args["v"], args["bt"], args["maxp"], args["sl"],
+                              args["tk"], args["tv"], args["path"], args["n"], args["sl_out"],
+                              args["B"], args["Hkv"], args["d"], args["T"], args["P"],
+                              args["num_pages"], args["status"], None)
+
+
+def test_kv_commit_host_checks(lib):
+    for kw in (dict(d=96), dict(T=0), dict(T=65), dict(P=48), dict(maxp=0), dict(num_pages=0),
+               dict(Hkv=0), dict(sl_out=A16)):          # seq_lens_out aliasing seq_lens
+        assert _commit(lib, **kw) == -2, kw
+    for name in ("k", "v", "bt", "sl", "path", "n"):
+        assert _commit(lib, **{name: None}) == -1, name
+    assert _commit(lib, tk=None) == -1                 # tree_k / tree_v: both or neither
+    assert _commit(lib, k=A16 + 8) == -3
+    assert _commit(lib, tk=A16 + 8) == -3
+    assert _commit(lib, B=0, k=None) == 0

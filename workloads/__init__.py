@@ -197,13 +197,16 @@ def make_workload(cfg: Config, seed: Optional[int] = None, *,
                   extra_pages: int = 0,
                   q_zero: bool = False,
                   per_sequence_trees: bool = False,
-                  tree_in_cache: bool = False) -> Workload:
+                  tree_in_cache: bool = False,
+                  tree_room: bool = False) -> Workload:
     """Build the seeded inputs of ``cfg`` (recipe in the module docstring).
 
     ``seq_lens`` / ``parents`` override the drawn values (edge-case tests);
     ``max_pages_per_seq`` widens the block table; ``extra_pages`` adds unused
     physical pages; ``q_zero`` zeroes the queries (closed-form tests);
-    ``per_sequence_trees`` / ``tree_in_cache`` select the layout variants.
+    ``per_sequence_trees`` / ``tree_in_cache`` select the layout variants;
+    ``tree_room`` maps pages for ``L_b + T`` positions without writing the
+    tree there (room for committing an accepted path).
     """
     gen = torch.Generator("cpu")
     gen.manual_seed(cfg.seed if seed is None else seed)
@@ -232,7 +235,7 @@ def make_workload(cfg: Config, seed: Optional[int] = None, *,
     else:
         parents_t = draw_tree()
 
-    span = cfg.T if tree_in_cache else 0
+    span = cfg.T if (tree_in_cache or tree_room) else 0
     pages_per = [(int(x) + span + P - 1) // P for x in sl.tolist()]
     used_pages = sum(pages_per)
     num_pages = used_pages + extra_pages
