@@ -18,6 +18,11 @@ Pins (what ties the oracle to something other than itself) live in
 * merge: split + merge over random disjoint chunks == single pass (1e-12);
 * mutation checks: planted mistakes in a copy of the C source fail a pin.
 
+* one-pass attention under an explicit mask (``dense_rows``) and the
+  explicit mask itself (``dense_mask``): equal to the split definition on the
+  same inputs (1e-12), a single visible key returns that key's value, and a
+  random mask against a NumPy textbook softmax.
+
 Parity unpinned: none of the value-producing functions is unpinned.
 """
 from __future__ import annotations
@@ -55,6 +60,7 @@ _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u64p = ctypes.POINTER(ctypes.c_uint64)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def _ptr(a: np.ndarray, t):
@@ -80,6 +86,12 @@ class Oracle:
         lib.oracle_merge.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_int, _f64p, _f64p,
                                      _f64p, _f64p]
         lib.oracle_merge.restype = None
+        lib.oracle_dense_rows.argtypes = [_u16p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p,
+                                          _u8p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_double, _i32p, ctypes.c_long,
+                                          _f64p, _f64p]
+        lib.oracle_dense_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -158,6 +170,30 @@ class Oracle:
         lse = np.zeros(n, dtype=np.float64)
         self.lib.oracle_merge(C, n, d, _ptr(outs, _f64p), _ptr(lses, _f64p),
                               _ptr(out, _f64p), _ptr(lse, _f64p))
+        return out, lse
+
+    # ---- one pass under an explicit mask (the naive form) -----------------
+    def dense_rows(self, wl, key_lens, dense, rows) -> Tuple[np.ndarray, np.ndarray]:
+        """(out [n][d], lse [n]) in float64: row (b, i, h) attends cache
+        position p < key_lens[b] where dense[b][i][p] != 0."""
+        from workloads import bf16_bits
+        c = wl.cfg
+        q, k, v = bf16_bits(wl.q), bf16_bits(wl.k_pages), bf16_bits(wl.v_pages)
+        bt = np.ascontiguousarray(wl.block_table.numpy().astype(np.int32))
+        kl = np.ascontiguousarray(np.asarray(key_lens, dtype=np.int32))
+        dm = np.ascontiguousarray(np.asarray(dense, dtype=np.uint8))
+        assert dm.shape[:2] == (c.B, c.T)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+        n = rows.shape[0]
+        out = np.zeros((n, c.d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        rc = self.lib.oracle_dense_rows(
+            _ptr(q, _u16p), _ptr(k, _u16p), _ptr(v, _u16p), _ptr(bt, _i32p),
+            wl.max_pages_per_seq, _ptr(kl, _i32p), _ptr(dm, _u8p), dm.shape[2], c.B, c.Hq, c.Hkv,
+            c.d, c.T, c.page, wl.num_pages, float(wl.scale), _ptr(rows, _i32p), n,
+            _ptr(out, _f64p), _ptr(lse, _f64p))
+        if rc != 0:
+            raise ValueError(f"oracle_dense_rows failed (code {rc})")
         return out, lse
 
     def max_threads(self) -> int:

@@ -276,6 +276,83 @@ int oracle_chunk_rows(const uint16_t *q, const uint16_t *k_pages, const uint16_t
 }
 
 /*
+ * Tree attention in one pass with an explicit mask: the "naive" form that
+ * split tree attention replaces (pith.science review of 2508.08192, "What
+ * carries the argument": instead of one attention under a giant explicit mask,
+ * the prefix and the tree are attended separately and merged).
+ *
+ * Every key sits in the paged cache -- the tree tokens too, at positions
+ * L_b .. L_b + T - 1 ("paged KV with tree padding", pith.science verdict
+ * record, desk editor's note) -- and query row (b, i, h) attends key
+ * position p in [0, key_lens[b]) exactly when dense[(b * T + i) * cols + p]
+ * is non-zero.  Same score, log-sum-exp and value sum as attend_chunk,
+ * written out again on its own.  Returns 0 or the first error code.
+ */
+int oracle_dense_rows(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                      const int32_t *block_table, int max_pages_per_seq,
+                      const int32_t *key_lens, const uint8_t *dense, long cols, int B, int Hq,
+                      int Hkv, int d, int T, int P, int num_pages, double scale,
+                      const int32_t *rows, long n_rows, double *out, double *lse) {
+    if (B < 0 || T < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || P < 1 || cols < 0)
+        return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    long max_n = 0;
+    for (int b = 0; b < B; ++b) {
+        if (key_lens[b] < 0 || key_lens[b] > cols) return ORACLE_BAD_ARG;
+        if (key_lens[b] > max_n) max_n = key_lens[b];
+    }
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_n + 1));
+    long *pos = (long *)malloc(sizeof(long) * (size_t)(max_n + 1));
+    double *qv = (double *)malloc(sizeof(double) * (size_t)d);
+    int err = (s && pos && qv) ? ORACLE_OK : ORACLE_NO_MEMORY;
+    for (long r = 0; r < n_rows && err == ORACLE_OK; ++r) {
+        const int b = rows[3 * r], i = rows[3 * r + 1], h = rows[3 * r + 2];
+        if (b < 0 || b >= B || i < 0 || i >= T || h < 0 || h >= Hq) { err = ORACLE_BAD_ARG; break; }
+        const int kvh = h / G;
+        const uint8_t *allow = dense + ((size_t)b * T + i) * (size_t)cols;
+        const uint16_t *qp = q + (((size_t)b * T + i) * Hq + h) * d;
+        for (int x = 0; x < d; ++x) qv[x] = bf16_to_double(qp[x]);
+        long n = 0;
+        for (long p = 0; p < key_lens[b] && err == ORACLE_OK; ++p) {
+            if (!allow[p]) continue;
+            if (p / P >= max_pages_per_seq) { err = ORACLE_BAD_ARG; break; }
+            const int32_t page = block_table[(size_t)b * max_pages_per_seq + p / P];
+            if (page < 0 || page >= num_pages) { err = ORACLE_BAD_PAGE; break; }
+            const uint16_t *kp = k_pages + (((size_t)page * Hkv + kvh) * P + p % P) * d;
+            double dot = 0.0;
+            for (int x = 0; x < d; ++x) dot += qv[x] * bf16_to_double(kp[x]);
+            s[n] = scale * dot;
+            pos[n] = p;
+            ++n;
+        }
+        if (err != ORACLE_OK) break;
+        double *o = out + (size_t)r * d;
+        for (int x = 0; x < d; ++x) o[x] = 0.0;
+        if (n == 0) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double mu = s[0];
+        for (long k = 1; k < n; ++k) mu = s[k] > mu ? s[k] : mu;
+        double Z = 0.0;
+        for (long k = 0; k < n; ++k) Z += exp(s[k] - mu);
+        const double L = mu + log(Z);
+        lse[r] = L;
+        for (long k = 0; k < n; ++k) {
+            const long p = pos[k];
+            const int32_t page = block_table[(size_t)b * max_pages_per_seq + p / P];
+            const uint16_t *vp = v_pages + (((size_t)page * Hkv + kvh) * P + p % P) * d;
+            const double w = exp(s[k] - L);
+            for (int x = 0; x < d; ++x) o[x] += w * bf16_to_double(vp[x]);
+        }
+    }
+    free(s);
+    free(pos);
+    free(qv);
+    return err;
+}
+
+/*
  * merge_attentions over disjoint key chunks (pith.science verdict record,
  * supporting_citations: Hydragen, Juravsky et al.; the same identity as the
  * chunked softmax of Rabe & Staats).  Given per-chunk normalised outputs

@@ -278,6 +278,98 @@ def pin_page_renumbering(orc, seed=18):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+# ---------------------------------------------------------------------------
+# one pass under an explicit mask (the naive form split attention replaces)
+# ---------------------------------------------------------------------------
+def _paged_tree_workload(seed):
+    return pin_workload(seed, tree_in_cache=True)
+
+
+def pin_onepass_equals_split(orc, dense_mod=None):
+    """With the tree in the cache, one pass under the explicit mask equals
+    split tree attention (the identity the pages' two-pass design rests on)."""
+    if dense_mod is None:
+        import oracle.dense as dense_mod
+    for seed, per_seq in ((19, False), (20, True)):
+        wl = pin_workload(seed, tree_in_cache=True, per_sequence_trees=per_seq)
+        c = wl.cfg
+        cols = 64 * ((max(wl.seq_lens.tolist()) + c.T + 63) // 64)
+        if per_seq:
+            masks = np.stack([paths_mask(wl.parents[b].tolist()) for b in range(c.B)])
+        else:
+            masks = paths_mask(wl.parents.tolist())
+        dense, key_lens = dense_mod.dense_mask(masks, wl.seq_lens.numpy(), c.T, cols)
+        assert np.array_equal(key_lens, wl.seq_lens.numpy() + c.T)
+        from oracle import all_rows
+        rows = all_rows(c.B, c.T, c.Hq)
+        got_o, got_l = orc.dense_rows(wl, key_lens, dense, rows)
+        for b in range(c.B):
+            sb = wl.sequence(b)
+            mb = masks[b] if per_seq else masks
+            ref_o, ref_l = dense_reference(sb, mb)
+            sel = rows[:, 0] == b
+            np.testing.assert_allclose(got_o[sel], ref_o.reshape(-1, c.d), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(got_l[sel], ref_l.reshape(-1), rtol=0, atol=1e-12)
+
+
+def pin_onepass_random_mask(orc, seed=21):
+    """An arbitrary explicit mask (some rows fully hidden) against a NumPy
+    textbook softmax over K/V gathered position by position."""
+    wl = _paged_tree_workload(seed)
+    c = wl.cfg
+    rng = np.random.default_rng(seed)
+    key_lens = wl.seq_lens.numpy() + c.T
+    cols = int(key_lens.max()) + 5
+    dense = (rng.random((c.B, c.T, cols)) < 0.5).astype(np.uint8)
+    dense[1, 2, :] = 0                       # a row that sees nothing
+    from oracle import all_rows
+    rows = all_rows(c.B, c.T, c.Hq)
+    got_o, got_l = orc.dense_rows(wl, key_lens, dense, rows)
+    kp = wl.k_pages.to(torch.float64).numpy()
+    vp = wl.v_pages.to(torch.float64).numpy()
+    qf = wl.q.to(torch.float64).numpy()
+    G = c.Hq // c.Hkv
+    for r, (b, i, h) in enumerate(rows):
+        ps = [p for p in range(int(key_lens[b])) if dense[b, i, p]]
+        if not ps:
+            assert got_l[r] == -math.inf and not got_o[r].any()
+            continue
+        pages = [int(wl.block_table[b, p // c.page]) for p in ps]
+        K = np.stack([kp[pg, h // G, p % c.page] for pg, p in zip(pages, ps)])
+        V = np.stack([vp[pg, h // G, p % c.page] for pg, p in zip(pages, ps)])
+        sc = K @ qf[b, i, h] * wl.scale
+        e = np.exp(sc - sc.max())
+        np.testing.assert_allclose(got_o[r], (e / e.sum()) @ V, rtol=0, atol=1e-12)
+        assert abs(got_l[r] - (sc.max() + math.log(e.sum()))) < 1e-12
+
+
+def pin_onepass_single_key(orc, seed=22):
+    """One visible key: out is that key's value exactly, lse its score."""
+    wl = _paged_tree_workload(seed)
+    c = wl.cfg
+    key_lens = wl.seq_lens.numpy() + c.T
+    cols = int(key_lens.max())
+    dense = np.zeros((c.B, c.T, cols), dtype=np.uint8)
+    pick = {}
+    for b in range(c.B):
+        for i in range(c.T):
+            p = (7 * b + 3 * i) % int(key_lens[b])
+            dense[b, i, p] = 1
+            pick[(b, i)] = p
+    from oracle import all_rows
+    rows = all_rows(c.B, c.T, c.Hq)
+    got_o, got_l = orc.dense_rows(wl, key_lens, dense, rows)
+    G = c.Hq // c.Hkv
+    for r, (b, i, h) in enumerate(rows):
+        p = pick[(b, i)]
+        pg = int(wl.block_table[b, p // c.page])
+        v = wl.v_pages[pg, h // G, p % c.page].to(torch.float64).numpy()
+        k = wl.k_pages[pg, h // G, p % c.page].to(torch.float64).numpy()
+        assert np.array_equal(got_o[r], v)
+        assert abs(got_l[r] - wl.scale * float(k @ wl.q[b, i, h].to(torch.float64).numpy())) \
+            < 1e-12
+
+
 ALL_PINS = [
     pin_mask_bruteforce,
     pin_dense_random_tree,
@@ -287,4 +379,7 @@ ALL_PINS = [
     pin_constant_values,
     pin_split_merge,
     pin_page_renumbering,
+    pin_onepass_equals_split,
+    pin_onepass_random_mask,
+    pin_onepass_single_key,
 ]

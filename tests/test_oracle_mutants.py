@@ -29,6 +29,11 @@ MUTANTS = {
     "mask_walk_drops_root": ("while (node != -1) {", "while (node > 0) {"),
     "merge_weight_unnormalised": ("const double w = exp(v - total);",
                                   "const double w = exp(v - top);"),
+    "dense_rows_transposed": ("dense + ((size_t)b * T + i) * (size_t)cols",
+                              "dense + ((size_t)i * B + b) * (size_t)cols"),
+    "dense_drops_last_key": ("p < key_lens[b] && err == ORACLE_OK", "p + 1 < key_lens[b] && err == ORACLE_OK"),
+    "dense_gqa_head_map": ("const int kvh = h / G;", "const int kvh = h % Hkv;"),
+    "dense_value_from_rank": ("const long p = pos[k];", "const long p = k;"),
     "logical_page_as_physical": (
         "int32_t page = c->block_table[(size_t)b * c->max_pages_per_seq + slot];",
         "int32_t page = (int32_t)slot;"),
@@ -57,3 +62,28 @@ def test_mutant_is_caught(name, tmp_path):
             failures.append(pin.__name__)
     assert failures, f"mutant {name} passed every pin"
     shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+DENSE_MUTANTS = {
+    "prefix_one_short": ("for p in range(L[b]):", "for p in range(L[b] - 1):"),
+    "tree_bits_unshifted": ("dense[b, i, L[b] + j] = 1", "dense[b, i, j] = 1"),
+    "tree_bit_order_reversed": ("if (bits >> j) & 1:", "if (bits >> (T - 1 - j)) & 1:"),
+    "key_lens_without_tree": ("[x + T for x in L]", "[x for x in L]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DENSE_MUTANTS))
+def test_dense_mask_mutant_is_caught(name, tmp_path, oracle):
+    import importlib.util
+    import oracle.dense as dense
+    before, after = DENSE_MUTANTS[name]
+    src = open(dense.__file__).read()
+    assert before in src, name
+    path = os.path.join(tmp_path, "dense_mutant.py")
+    with open(path, "w") as f:
+        f.write(src.replace(before, after))
+    spec = importlib.util.spec_from_file_location("dense_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        pins.pin_onepass_equals_split(oracle, dense_mod=mod)
