@@ -58,10 +58,13 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", choices=sorted(CONFIGS), default="llama8b")
-    p.add_argument("--layout", choices=["shared", "per_seq", "paged_tree"], default="shared",
+    p.add_argument("--layout", choices=["shared", "per_seq", "paged_tree", "full_mask"],
+                   default="shared",
                    help="shared: one draft tree for the batch, tree K/V in their own buffers; "
                         "per_seq: one tree per sequence; paged_tree: tree K/V padded into the "
-                        "paged cache at positions L_b + j")
+                        "paged cache at positions L_b + j; full_mask: the one-pass ablation "
+                        "(paged_tree layout, explicit [B][T][L+T] mask, no split into prefix "
+                        "and tree passes)")
     p.add_argument("--path", choices=["verify", "accept_commit"], default="verify",
                    help="verify: the split tree attention step (default); accept_commit: "
                         "greedy acceptance of the verified tree plus the KV commit of the "
@@ -109,7 +112,7 @@ def workload_desc(cfg, layout="shared"):
 
 def make_layout_workload(cfg, layout, seed=None):
     return make_workload(cfg, seed=seed, per_sequence_trees=(layout == "per_seq"),
-                         tree_in_cache=(layout == "paged_tree"))
+                         tree_in_cache=(layout in ("paged_tree", "full_mask")))
 
 
 def algorithmic_bytes(wl):
@@ -206,13 +209,25 @@ def emit(obj):
 # ---------------------------------------------------------------------------
 # CPU side: the fp64 oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_token_fn(wl):
+def oracle_token_fn(wl, layout="shared"):
     """f(b, i): the oracle on one tree token (all Hq query heads of sequence b,
-    node i), with sequence b's own tree mask."""
+    node i), with sequence b's own tree mask (the one-pass oracle under the
+    explicit mask for the full_mask layout)."""
     import oracle
     orc = oracle.get()
     c = wl.cfg
     threads = len(os.sched_getaffinity(0))
+    if layout == "full_mask":
+        from oracle.dense import dense_mask
+        tm = orc.tree_mask(wl.parents.tolist())
+        cols = int(wl.seq_lens.max()) + c.T
+        dense, key_lens = dense_mask(tm, wl.seq_lens.numpy(), c.T, cols)
+
+        def f_dense(b, i):
+            rows = np.array([(b, i, h) for h in range(c.Hq)], dtype=np.int32)
+            orc.dense_rows(wl, key_lens, dense, rows)
+
+        return f_dense, 1
     if wl.parents.dim() == 2:
         seqs = [wl.sequence(b) for b in range(c.B)]
         masks = [orc.tree_mask(s.parents.tolist()) for s in seqs]
@@ -230,11 +245,11 @@ def oracle_token_fn(wl):
     return f, threads
 
 
-def oracle_tokens_per_s(wl, budget_s, max_tokens=None):
+def oracle_tokens_per_s(wl, budget_s, max_tokens=None, layout="shared"):
     """Time the oracle on whole tree tokens (all Hq heads of one (b, i)),
     round-robin over the batch, until `budget_s` of wall time is spent."""
     c = wl.cfg
-    f, threads = oracle_token_fn(wl)
+    f, threads = oracle_token_fn(wl, layout)
     tokens = [(b, i) for b in range(c.B) for i in range(c.T)]
     done = 0
     t0 = time.perf_counter()
@@ -253,7 +268,7 @@ def run_reference(args):
         return
     cfg = CONFIGS[args.config]
     wl = make_layout_workload(cfg, args.layout)
-    f, threads = oracle_token_fn(wl)
+    f, threads = oracle_token_fn(wl, args.layout)
     tokens = [(b, i) for b in range(cfg.B) for i in range(cfg.T)]
 
     def step(n):
@@ -316,10 +331,20 @@ def run_ours(args):
     ws_bytes = ta.workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.T, 0, cfg.page)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if layout == "full_mask":
+        cols = ta.dense_cols_for(int(wl.seq_lens.max()) + cfg.T)
+        dense = torch.empty((cfg.B, cfg.T, cols), dtype=torch.uint8, device=dev)
+        key_lens = torch.empty(cfg.B, dtype=torch.int32, device=dev)
 
     def hot_path(par, q_, k_, v_, bt_, sl_, tk_, tv_):
-        """One pass of the whole path: masks, then split tree attention."""
-        if layout == "per_seq":
+        """One pass of the whole path: masks, then tree attention."""
+        if layout == "full_mask":
+            ta.mask_build(par, mask_out=mask, status=status)
+            ta.dense_mask_build(mask, sl_, cfg.T, cols, dense_out=dense, key_lens=key_lens,
+                                status=status)
+            ta.verify_dense(q_, k_, v_, bt_, key_lens, dense, out=out, lse=lse, workspace=ws,
+                            status=status, softmax_scale=wl.scale)
+        elif layout == "per_seq":
             ta.mask_build_batched(par, mask_out=mask, status=status)
             ta.verify_batched(q_, k_, v_, bt_, sl_, tk_, tv_, mask, out=out, lse=lse,
                               workspace=ws, status=status, softmax_scale=wl.scale)
@@ -336,6 +361,10 @@ def run_ours(args):
         hot_path(parents, q, kps[r % R], vps[r % R], bt, sl, tk, tv)
 
     def prefix_only(r):
+        if layout == "full_mask":   # the one-pass kernel has no separate entry: time the call
+            ta.verify_dense(q, kps[r % R], vps[r % R], bt, key_lens, dense, out=out, lse=lse,
+                            workspace=ws, status=status, softmax_scale=wl.scale)
+            return
         ta.prefix_pass(q, kps[r % R], vps[r % R], bt, sl, ws, status=status,
                        softmax_scale=wl.scale)
 
@@ -416,7 +445,7 @@ def run_ours(args):
         host = dict(parents=wl.parents, q=wl.q, k=wl.k_pages, v=wl.v_pages, bt=wl.block_table,
                     sl=wl.seq_lens, tk=wl.tree_k, tv=wl.tree_v)
         d = dict(parents=parents, q=q, k=kps[0], v=vps[0], bt=bt, sl=sl, tk=tk, tv=tv)
-        if layout == "paged_tree":   # the tree K/V travel inside the pages
+        if layout in ("paged_tree", "full_mask"):   # the tree K/V travel inside the pages
             del host["tk"], host["tv"]
         h = {k: v.pin_memory() for k, v in host.items()}
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -450,7 +479,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, n_tok, el, threads = oracle_tokens_per_s(wl, args.cpu_seconds)
+        v, n_tok, el, threads = oracle_tokens_per_s(wl, args.cpu_seconds, layout=layout)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n_tok} tree tokens (all {cfg.Hq} query heads each) of this "
                          f"workload, round-robin, {el:.1f} s of fp64 oracle time"}
@@ -468,7 +497,9 @@ def run_ours(args):
             "us_per_call": ms_step * 1e3,
             "call_hbm_gbs": nbytes["call"] / (ms_step * 1e-3) / 1e9,
             "prefix_kernel_us": ms_prefix * 1e3,
-            "roofline": {"bound": "hbm", "kernel": "prefix_pass_kernel",
+            "roofline": {"bound": "hbm",
+                         "kernel": "prefix_pass_kernel" if layout != "full_mask" else
+                         "prefix_pass_kernel (explicit mask) + merge, timed together",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes["prefix_kernel"],

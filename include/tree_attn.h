@@ -210,6 +210,42 @@ TREE_ATTN_API int tree_attn_verify_paged_tree(const uint16_t *q, const uint16_t 
                                               int32_t *status, void *stream);
 
 /*
+ * tree_dense_mask_build / tree_attn_verify_dense -- the one-pass form of tree
+ * attention under an explicit mask: the "giant explicit mask" that split tree
+ * attention replaces (pith.science review of arXiv 2508.08192, "What carries
+ * the argument").  Kept as an ablation of the split form; both compute the
+ * same attention.  The tree tokens must sit in the paged cache after each
+ * prefix (tree_attn_verify_paged_tree layout).
+ *
+ * tree_dense_mask_build writes dense_mask uint8 [B][T][dense_cols]:
+ *   dense_mask[b][t][p] = 1 for p < seq_lens[b] (the committed prefix),
+ *                       = bit (p - seq_lens[b]) of mask[t] for the tree tokens,
+ *                       = 0 beyond;
+ * and key_lens[b] = seq_lens[b] + T.  dense_cols must be a multiple of 16
+ * and at least max_b seq_lens[b] + T (else status TREE_ATTN_STATUS_BAD_SEQ_LEN).
+ * mask: uint64 [T] (mask_stride 0) or [B][T] (mask_stride T).
+ *
+ * tree_attn_verify_dense attends, for query (b, t, h), every cache position
+ * p < key_lens[b] with dense_mask[b][t][p] != 0, in one pass (the prefix
+ * kernel's split over the key range and the LSE merge still apply; there is
+ * no separate tree pass).  Arguments otherwise as tree_attn_verify; the
+ * workspace size is tree_attn_workspace_size's.  Returns as tree_attn_verify.
+ */
+TREE_ATTN_API int tree_dense_mask_build(const uint64_t *mask, int mask_stride,
+                                        const int32_t *seq_lens, int B, int T, int dense_cols,
+                                        uint8_t *dense_mask, int32_t *key_lens, int32_t *status,
+                                        void *stream);
+
+TREE_ATTN_API int tree_attn_verify_dense(const uint16_t *q, const uint16_t *k_pages,
+                                         const uint16_t *v_pages, const int32_t *block_table,
+                                         int max_pages_per_seq, const int32_t *key_lens,
+                                         const uint8_t *dense_mask, int dense_cols, uint16_t *out,
+                                         float *lse, int B, int Hq, int Hkv, int d, int T,
+                                         int page_size, int num_pages, float softmax_scale,
+                                         void *workspace, size_t workspace_bytes, int32_t *status,
+                                         void *stream);
+
+/*
  * tree_greedy_accept -- greedy acceptance of the verified draft tree
  * ("Efficient Speculative Decoding for Llama at Scale", fdeinterviews.com
  * summary, opening paragraph: the service commits one accepted path; greedy

@@ -29,6 +29,9 @@ from ._lib import (  # noqa: F401
     verify_batched,
     verify_paged_tree,
     greedy_accept,
+    dense_cols_for,
+    dense_mask_build,
+    verify_dense,
     kv_commit,
     version,
     workspace_size,

@@ -49,6 +49,8 @@ EXPORTED = (
     "tree_attn_verify_paged_tree",
     "tree_greedy_accept",
     "tree_kv_commit",
+    "tree_dense_mask_build",
+    "tree_attn_verify_dense",
 )
 
 
@@ -105,6 +107,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_kv_commit.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                    i32, i32, vp, vp]
     lib.tree_kv_commit.restype = i32
+    lib.tree_dense_mask_build.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp]
+    lib.tree_dense_mask_build.restype = i32
+    lib.tree_attn_verify_dense.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, i32, i32,
+                                           i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
+    lib.tree_attn_verify_dense.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -308,6 +315,63 @@ def _verify_generic(fn, q, k_pages, v_pages, block_table, seq_lens, tree_k, tree
         _ptr(status), _stream_handle(stream))
     if rc != 0:
         raise TreeAttnError(fn, rc)
+    return out, lse
+
+
+def dense_cols_for(max_keys: int) -> int:
+    """Row length of an explicit mask covering max_keys cache positions."""
+    return max(16, (int(max_keys) + 15) // 16 * 16)
+
+
+def dense_mask_build(mask, seq_lens, T: int, dense_cols: int, *, dense_out=None, key_lens=None,
+                     status=None, stream=None):
+    """Explicit [B][T][dense_cols] mask of the one-pass form (tree tokens in
+    the cache after each prefix) and key_lens = seq_lens + T."""
+    _check(mask, "mask", _BITS64)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    B = seq_lens.shape[0]
+    dev = seq_lens.device
+    if dense_out is None:
+        dense_out = torch.empty((B, T, dense_cols), dtype=torch.uint8, device=dev)
+    if key_lens is None:
+        key_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    stride = T if mask.dim() == 2 else 0
+    rc = load().tree_dense_mask_build(_ptr(mask), stride, _ptr(seq_lens), B, T, dense_cols,
+                                      _ptr(dense_out), _ptr(key_lens), _ptr(status),
+                                      _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_dense_mask_build", rc)
+    return dense_out, key_lens
+
+
+def verify_dense(q, k_pages, v_pages, block_table, key_lens, dense_mask, *, out=None, lse=None,
+                 workspace=None, status=None, softmax_scale=None, stream=None):
+    """One-pass tree attention under the explicit mask dense_mask [B][T][cols]."""
+    bf = (torch.bfloat16,)
+    _check(q, "q", bf, 4)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(key_lens, "key_lens", (torch.int32,), 1)
+    _check(dense_mask, "dense_mask", (torch.uint8,), 3)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, d, T, 0, P)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = load().tree_attn_verify_dense(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+        _ptr(key_lens), _ptr(dense_mask), dense_mask.shape[2], _ptr(out), _ptr(lse), B, Hq, Hkv,
+        d, T, P, num_pages, float(softmax_scale), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_verify_dense", rc)
     return out, lse
 
 

@@ -174,6 +174,11 @@ struct PrefixArgs {
     int32_t* status;
     int B, Hq, Hkv, G, T, M, RB, P, max_pages, num_pages, n_ctas;
     float scale_log2;
+    // One-pass form under an explicit mask (DENSE kernels only): key p of
+    // query token t of sequence b is visible when dense[(b*T + t)*dense_cols + p]
+    // is non-zero; seq_lens then counts every key in the cache, tree included.
+    const uint8_t* dense;
+    int dense_cols;
 };
 
 __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
@@ -254,7 +259,7 @@ __device__ __forceinline__ int blocks_of(const Segment& sg) {
     return (sg.chunk_end - sg.chunk_begin + 1) / 2;
 }
 
-template <int D, int F>
+template <int D, int F, bool DENSE>
 __global__ void __launch_bounds__(192, 1)
     prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefixArgs a) {
@@ -548,11 +553,35 @@ __global__ void __launch_bounds__(192, 1)
             const int L = clamp_seq_len(a.seq_lens[cur.b], a.P, a.max_pages, bad);
             float m_ref = kNegInf;  // base-2 reference; -inf until a key is seen
             float l_sum = 0.f;
+            // Explicit-mask form only: the sum of the probabilities as the
+            // P.V product sees them (bf16).  Such a row may hold just a few
+            // keys (tree tokens after an empty prefix), where the rounding
+            // of P does not average out; the epilogue rescales the row's
+            // accumulator by l_sum / l_rnd, so that out keeps a consistent
+            // numerator and denominator while lse keeps the exact sum.
+            float l_rnd = 0.f;
             for (int ch = cur.chunk_begin; ch < cur.chunk_end; ch += 2, ++jj) {
                 const bool first = ch == cur.chunk_begin;
                 const int nh = min(2, cur.chunk_end - ch);
                 const int n_valid = min(nh * kChunk, L - ch * kChunk);
                 const int nv = n_valid - k0;  // valid keys in this replica's range (may be <= 0)
+                // Explicit mask bytes of this row's keys, fetched before the
+                // scores are waited for (16 keys per vector).
+                uint4 mbits[DENSE ? KF / 16 : 1];
+                if constexpr (DENSE) {
+                    const int p0 = ch * kChunk + k0;
+                    const int lim = min(L, a.dense_cols);
+                    const uint8_t* mrow = a.dense;
+                    if (row_ok)
+                        mrow += (static_cast<size_t>(cur.b) * a.T + (cur.rb * kRows + lr) / a.G) *
+                                a.dense_cols;
+#pragma unroll
+                    for (int j = 0; j < KF / 16; ++j) {
+                        mbits[j] = make_uint4(0, 0, 0, 0);
+                        if (row_ok && p0 + 16 * j < lim)
+                            mbits[j] = __ldg(reinterpret_cast<const uint4*>(mrow + p0 + 16 * j));
+                    }
+                }
                 if (!wait_all(bar(S::S_FULL + (jj & 1)), (jj >> 1) & 1)) {
                     ok = false;
                     break;
@@ -573,6 +602,19 @@ __global__ void __launch_bounds__(192, 1)
                 // (scale > 0, so the max of the raw scores gives the max of x).
                 float alpha = 1.f;
                 bool rescale = false;
+                if constexpr (DENSE) {
+                    // Hidden keys score -inf: they add nothing to the max or
+                    // the sum, and their probabilities are exactly 0.
+#pragma unroll
+                    for (int i = 0; i < KF; ++i) {
+                        const uint4 w4 = mbits[i / 16];
+                        const uint32_t w = ((i % 16) / 4 == 0)   ? w4.x
+                                           : ((i % 16) / 4 == 1) ? w4.y
+                                           : ((i % 16) / 4 == 2) ? w4.z
+                                                                 : w4.w;
+                        if (((w >> (8 * (i % 4))) & 0xffu) == 0) s[i] = kNegInf;
+                    }
+                }
                 if (row_ok) {
                     // Eight independent partial maxima / sums keep the
                     // dependency chains short.
@@ -598,13 +640,27 @@ __global__ void __launch_bounds__(192, 1)
                         alpha = ptx::ex2(m_ref - mx);
                         m_ref = mx;
                         l_sum *= alpha;
+                        l_rnd *= alpha;
                         rescale = true;
                     }
                     const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;
                     float sp[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) sp[u] = 0.f;
-                    if (nv >= KF) {
+                    if constexpr (DENSE) {
+                        // Sum both the exact and the bf16-rounded values (see
+                        // the epilogue).
+                        float sr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int i = 0; i < KF; ++i) {
+                            const float e =
+                                (i < nv) ? ptx::ex2(fmaf(s[i], a.scale_log2, neg_m)) : 0.f;
+                            s[i] = __bfloat162float(__float2bfloat16_rn(e));
+                            sp[i & 7] += e;
+                            sr[i & 3] += s[i];
+                        }
+                        l_rnd += (sr[0] + sr[1]) + (sr[2] + sr[3]);
+                    } else if (nv >= KF) {
 #pragma unroll
                         for (int i = 0; i < KF; ++i) {
                             s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
@@ -694,6 +750,7 @@ __global__ void __launch_bounds__(192, 1)
             if (warp_any) {
                 float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
                 const uint32_t to = lane_base + S::TM_O;
+                const float acc_scale = (DENSE && l_rnd > 0.f) ? l_sum / l_rnd : 1.f;
                 float4* acc =
                     reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
 #pragma unroll
@@ -702,6 +759,10 @@ __global__ void __launch_bounds__(192, 1)
                     ptx::tmem_ld32(to + c, o);
                     ptx::tmem_wait_ld();
                     if (row_ok) {
+                        if constexpr (DENSE) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= acc_scale;
+                        }
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             acc[c / 4 + i] =
@@ -870,7 +931,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    if (active && sub == 0) {
+    if (active && sub == 0 && a.mask != nullptr) {
         float qv[E];
         load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
         uint64_t bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
@@ -1104,7 +1165,9 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        for (auto k : {prefix_pass_kernel<D, 1>, prefix_pass_kernel<D, 2>, prefix_pass_kernel<D, 4>}) {
+        for (auto k : {prefix_pass_kernel<D, 1, false>, prefix_pass_kernel<D, 2, false>,
+                       prefix_pass_kernel<D, 4, false>, prefix_pass_kernel<D, 1, true>,
+                       prefix_pass_kernel<D, 2, true>, prefix_pass_kernel<D, 4, true>}) {
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
             if (e != cudaSuccess) return e;
         }
@@ -1130,11 +1193,18 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.num_pages = v.num_pages;
     pa.n_ctas = v.n_ctas;
     pa.scale_log2 = v.scale_log2;
+    pa.dense = v.dense;
+    pa.dense_cols = v.dense_cols;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
     const int F = pa.RB == 1 ? replicas_of(M) : 1;
-    auto kernel = F == 4 ? prefix_pass_kernel<D, 4>
-                         : (F == 2 ? prefix_pass_kernel<D, 2> : prefix_pass_kernel<D, 1>);
+    auto kernel = F == 4 ? prefix_pass_kernel<D, 4, false>
+                         : (F == 2 ? prefix_pass_kernel<D, 2, false>
+                                   : prefix_pass_kernel<D, 1, false>);
+    if (v.dense != nullptr)
+        kernel = F == 4 ? prefix_pass_kernel<D, 4, true>
+                        : (F == 2 ? prefix_pass_kernel<D, 2, true>
+                                  : prefix_pass_kernel<D, 1, true>);
     return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, pa);
 }
 
@@ -1184,7 +1254,63 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     return launch_pdl(kernel, grid, dim3(32 * kMergeWarps), 0, stream, ma);
 }
 
+// ===========================================================================
+// Explicit mask of the one-pass form: row (b, t) over cache positions p:
+// 1 for the committed prefix (p < L_b), bit p - L_b of the tree mask for the
+// tree tokens padded after it, 0 beyond.  16 bytes per thread.
+// ===========================================================================
+__global__ void __launch_bounds__(256)
+    dense_mask_kernel(const uint64_t* __restrict__ mask, int mask_stride,
+                      const int32_t* __restrict__ seq_lens, int B, int T, int cols,
+                      uint8_t* __restrict__ dense, int32_t* __restrict__ key_lens,
+                      int32_t* __restrict__ status) {
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    const int row = blockIdx.x;  // b * T + t
+    const int b = row / T, t = row % T;
+    int L = seq_lens[b];
+    const bool bad = L < 0 || static_cast<long long>(L) + T > cols;
+    if (L < 0) L = 0;
+    uint64_t bits = mask[static_cast<size_t>(b) * mask_stride + t];
+    if (T < 64) bits &= (1ull << T) - 1ull;
+    const long long p0 = (static_cast<long long>(blockIdx.y) * blockDim.x + threadIdx.x) * 16;
+    if (p0 < cols) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const long long p = p0 + 4 * q + k;
+                uint32_t on = 0;
+                if (p < L)
+                    on = 1;
+                else if (p - L < T)
+                    on = static_cast<uint32_t>((bits >> (p - L)) & 1ull);
+                v |= on << (8 * k);
+            }
+            w[q] = v;
+        }
+        *reinterpret_cast<uint4*>(dense + static_cast<size_t>(row) * cols + p0) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        key_lens[b] = L + T;
+        if (bad) report(status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dense_mask_build(const uint64_t* mask, int mask_stride,
+                                    const int32_t* seq_lens, int B, int T, int dense_cols,
+                                    uint8_t* dense, int32_t* key_lens, int32_t* status,
+                                    cudaStream_t stream) {
+    const unsigned per_cta = 256 * 16;
+    const dim3 grid(static_cast<unsigned>(B) * T, (dense_cols + per_cta - 1) / per_cta);
+    return launch_pdl(dense_mask_kernel, grid, dim3(256), 0, stream, mask, mask_stride, seq_lens,
+                      B, T, dense_cols, dense, key_lens, status);
+}
 
 cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64_t* mask,
                               int32_t* status, cudaStream_t stream) {

@@ -26,7 +26,19 @@ struct VerifyArgs {
     float scale_log2;
     int mask_stride;    // 0: mask[T] shared by the batch; T: mask[B][T]
     int tree_in_cache;  // tree K/V at positions seq_lens[b] .. +T of the paged cache
+    // One pass under an explicit mask (uint8 [B][T][dense_cols]); seq_lens
+    // then counts every key in the cache and the merge has no suffix
+    // (mask == nullptr).  nullptr: the split form.
+    const uint8_t* dense;
+    int dense_cols;
 };
+
+// Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and
+// key_lens[b] = seq_lens[b] + T.
+cudaError_t launch_dense_mask_build(const uint64_t* mask, int mask_stride,
+                                    const int32_t* seq_lens, int B, int T, int dense_cols,
+                                    uint8_t* dense, int32_t* key_lens, int32_t* status,
+                                    cudaStream_t stream);
 
 // Enqueue the mask builder (one warp per tree, n_trees trees of T nodes).
 cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64_t* mask,

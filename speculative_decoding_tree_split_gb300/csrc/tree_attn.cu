@@ -231,11 +231,17 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
                   int mask_stride, bool tree_in_cache, uint16_t* out, float* lse, int B, int Hq,
                   int Hkv, int d, int T, int page_size, int num_pages, float softmax_scale,
                   void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
-                  int n_ctas) {
+                  int n_ctas, const uint8_t* dense = nullptr, int dense_cols = 0) {
     if (mask_stride != 0 && mask_stride != T) return TREE_ATTN_ERR_SHAPE;
     if (tree_in_cache) {
         tree_k = k_pages;  // unused: keep the null checks below meaningful
         tree_v = v_pages;
+    }
+    if (dense != nullptr) {
+        // One pass under the explicit mask: no tree mask, no suffix.
+        if (dense_cols < 16 || dense_cols % 16 != 0) return TREE_ATTN_ERR_SHAPE;
+        if (!aligned(dense, 16)) return TREE_ATTN_ERR_ALIGN;
+        mask = reinterpret_cast<const uint64_t*>(dense);  // non-null for the checks below
     }
     int rc = check_common(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, softmax_scale);
     if (rc != TREE_ATTN_OK) return rc;
@@ -280,6 +286,9 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
     a.scale_log2 = to_log2(softmax_scale);
     a.mask_stride = mask_stride;
     a.tree_in_cache = tree_in_cache ? 1 : 0;
+    a.dense = dense;
+    a.dense_cols = dense_cols;
+    if (dense != nullptr) a.mask = nullptr;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = prefix_impl(a, k_pages, v_pages, st);
     if (rc != TREE_ATTN_OK) return rc;
@@ -327,6 +336,37 @@ int tree_attn_verify_paged_tree(const uint16_t* q, const uint16_t* k_pages,
                          nullptr, mask, mask_stride, true, out, lse, B, Hq, Hkv, d, T,
                          page_size, num_pages, softmax_scale, workspace, workspace_bytes, status,
                          stream, 0);
+}
+
+int tree_dense_mask_build(const uint64_t* mask, int mask_stride, const int32_t* seq_lens, int B,
+                          int T, int dense_cols, uint8_t* dense_mask, int32_t* key_lens,
+                          int32_t* status, void* stream) {
+    if (B < 0 || T < 1 || T > TREE_ATTN_MAX_T || (mask_stride != 0 && mask_stride != T) ||
+        dense_cols < 16 || dense_cols % 16 != 0 || dense_cols / (256 * 16) >= 65535)
+        return TREE_ATTN_ERR_SHAPE;
+    if (B == 0) return TREE_ATTN_OK;
+    if (!mask || !seq_lens || !dense_mask || !key_lens) return TREE_ATTN_ERR_NULL;
+    if (!aligned(mask, 8) || !aligned(seq_lens, 4) || !aligned(dense_mask, 16) ||
+        !aligned(key_lens, 4) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    return launch_dense_mask_build(mask, mask_stride, seq_lens, B, T, dense_cols, dense_mask,
+                                   key_lens, status, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TREE_ATTN_OK
+               : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_attn_verify_dense(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                           const int32_t* block_table, int max_pages_per_seq,
+                           const int32_t* key_lens, const uint8_t* dense_mask, int dense_cols,
+                           uint16_t* out, float* lse, int B, int Hq, int Hkv, int d, int T,
+                           int page_size, int num_pages, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, int32_t* status, void* stream) {
+    if (dense_mask == nullptr) return TREE_ATTN_ERR_NULL;
+    return verify_common(q, k_pages, v_pages, block_table, max_pages_per_seq, key_lens, nullptr,
+                         nullptr, nullptr, 0, true, out, lse, B, Hq, Hkv, d, T, page_size,
+                         num_pages, softmax_scale, workspace, workspace_bytes, status, stream, 0,
+                         dense_mask, dense_cols);
 }
 
 int tree_attn_verify(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,

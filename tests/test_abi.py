@@ -192,3 +192,25 @@ def test_kv_commit_host_checks(lib):
     assert _commit(lib, k=A16 + 8) == -3
     assert _commit(lib, tk=A16 + 8) == -3
     assert _commit(lib, B=0, k=None) == 0
+
+
+def test_dense_entries_host_checks(lib):
+    a = A16
+    f = lib.tree_dense_mask_build
+    assert f(a, 0, a, 2, 4, 15, a, a, None, None) == -2      # cols not a multiple of 16
+    assert f(a, 3, a, 2, 4, 64, a, a, None, None) == -2      # stride neither 0 nor T
+    assert f(a, 0, a, 2, 65, 64, a, a, None, None) == -2
+    assert f(None, 0, a, 2, 4, 64, a, a, None, None) == -1
+    assert f(a, 0, a, 2, 4, 64, a + 8, a, None, None) == -3  # dense rows need 16 B alignment
+    assert f(a, 0, a, 0, 4, 64, None, None, None, None) == 0
+    v = lib.tree_attn_verify_dense
+    base = [a, a, a, a, 4, a, a, 64, a, a, 2, 8, 2, 128, 4, 64, 8, 0.1, a, 1 << 30, None, None]
+    args = list(base)
+    args[6] = None
+    assert v(*args) == -1
+    args = list(base)
+    args[7] = 40
+    assert v(*args) == -2
+    args = list(base)
+    args[6] = a + 4
+    assert v(*args) == -3
