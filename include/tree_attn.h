@@ -302,6 +302,29 @@ TREE_ATTN_API int tree_kv_commit(uint16_t *k_pages, uint16_t *v_pages, const int
                                  int page_size, int num_pages, int32_t *status, void *stream);
 
 /*
+ * tree_attn_plan -- the kernel selector's choices for a call of these shapes
+ * (the split-count heuristic of flash-decoding, Dao et al., cited in the
+ * pith.science verdict record's supporting_citations; here it sizes a
+ * persistent stream-K grid instead of a split count).  Host only; the
+ * verify entry points make the same choices.  Inputs as tree_attn_verify;
+ * sm_count_hint > 0 replaces the current device's SM count (no CUDA call is
+ * then made).  Returns 0, -1 (out NULL), -2 (shapes), -5 (no device).
+ */
+typedef struct tree_attn_plan_info {
+    int units;               /* B * Hkv * row_blocks work units                      */
+    int row_blocks;          /* ceil(T * Hq / Hkv / 128) query-row blocks per unit   */
+    int replicas;            /* query-row copies per 128-row tile (1, 2 or 4)         */
+    int n_ctas;              /* persistent prefix-pass CTAs                           */
+    int merge_warps_per_row; /* warps that merge one query row (1, 2 or 4)            */
+    long long max_steps;     /* 64-token work-line steps if every sequence were full */
+    size_t workspace_bytes;  /* partial-result slots for this n_ctas                 */
+} tree_attn_plan_info;
+
+TREE_ATTN_API int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size,
+                                 int max_pages_per_seq, int sm_count_hint,
+                                 tree_attn_plan_info *out);
+
+/*
  * tree_attn_prefix_pass / tree_attn_suffix_merge -- the two passes of
  * tree_attn_verify as separate calls (tree_attn_verify_ctas == prefix pass
  * then suffix merge, same arguments).  The prefix pass ("attention from query

@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     load,
     mask_build,
     mask_build_batched,
+    plan,
     prefix_pass,
     suffix_merge,
     verify,

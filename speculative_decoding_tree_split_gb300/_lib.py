@@ -51,7 +51,17 @@ EXPORTED = (
     "tree_kv_commit",
     "tree_dense_mask_build",
     "tree_attn_verify_dense",
+    "tree_attn_plan",
 )
+
+
+class PlanInfo(ctypes.Structure):
+    """tree_attn_plan_info of include/tree_attn.h."""
+
+    _fields_ = [("units", ctypes.c_int), ("row_blocks", ctypes.c_int),
+                ("replicas", ctypes.c_int), ("n_ctas", ctypes.c_int),
+                ("merge_warps_per_row", ctypes.c_int), ("max_steps", ctypes.c_longlong),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class TreeAttnError(RuntimeError):
@@ -112,6 +122,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_verify_dense.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, i32, i32,
                                            i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     lib.tree_attn_verify_dense.restype = i32
+    lib.tree_attn_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                   ctypes.POINTER(PlanInfo)]
+    lib.tree_attn_plan.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -316,6 +329,18 @@ def _verify_generic(fn, q, k_pages, v_pages, block_table, seq_lens, tree_k, tree
     if rc != 0:
         raise TreeAttnError(fn, rc)
     return out, lse
+
+
+def plan(B: int, Hq: int, Hkv: int, d: int, T: int, page_size: int, max_pages_per_seq: int,
+         sm_count: int = 0) -> dict:
+    """The kernel selector's launch choices for these shapes (host only when
+    sm_count > 0)."""
+    info = PlanInfo()
+    rc = load().tree_attn_plan(B, Hq, Hkv, d, T, page_size, max_pages_per_seq, sm_count,
+                               ctypes.byref(info))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_plan", rc)
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
 
 
 def dense_cols_for(max_keys: int) -> int:

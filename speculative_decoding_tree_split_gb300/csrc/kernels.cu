@@ -1240,12 +1240,10 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.block_table = v.block_table;
     ma.num_pages = v.num_pages;
     ma.status = v.status;
-    // Warps per row from the expected partials per row: prefix CTAs per unit
-    // (plus one for a straddled boundary) times the row copies.
-    const long long units = static_cast<long long>(v.B) * v.Hkv * RB;
-    const int F = RB == 1 ? replicas_of(M) : 1;
-    const long long expect = (v.n_ctas / units + 2) * F;
-    ma.wpr = expect > 12 ? 4 : (expect > 6 ? 2 : 1);
+    const Plan plan = make_plan(v.B, v.Hq, v.Hkv, v.T, v.P, v.max_pages, v.n_ctas, v.n_ctas);
+    const long long units = plan.units;
+    const int F = plan.F;
+    ma.wpr = plan.merge_wpr;
     const int rows = M < kRows ? M : kRows;
     const int rows_per_cta = kMergeWarps / ma.wpr;
     const dim3 grid(static_cast<unsigned>(units), (rows + rows_per_cta - 1) / rows_per_cta);

@@ -205,4 +205,46 @@ TA_HD int replicas_of(int M) { return M <= 32 ? 4 : (M <= 64 ? 2 : 1); }
 // Partial-result slot layout: m[kRows] | l[kRows] | acc[kRows][d] (fp32).
 TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>(kRows) * d; }
 
+// The kernel selector: every launch choice of a call, from the shapes alone
+// (the sequence lengths live on the device and are not read by the host).
+// Split-count heuristics pick a number of KV splits that fills the SMs from
+// the batch, head count and length (flash-decoding, Dao et al., cited by the
+// pith.science verdict record); here the work line is cut into equal
+// stretches for a persistent grid, so what remains to choose is:
+//   n_ctas     one persistent CTA per SM, but never more CTAs than the
+//              largest possible number of 64-token steps (small problems
+//              would otherwise launch CTAs with nothing to do);
+//   F          query-row copies per tile when one 128-row block holds the
+//              unit's rows (small M: the softmax work per CTA is split);
+//   merge_wpr  warps per query row in the merge, from the partials a row
+//              expects: prefix CTAs per unit (+2 for straddled ends) x F.
+struct Plan {
+    int G, M, RB, units, F, n_ctas, merge_wpr;
+    long long max_steps;
+};
+
+TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm_count,
+                     int n_ctas_req) {
+    Plan p;
+    p.G = Hq / Hkv;
+    p.M = T * p.G;
+    p.RB = (p.M + kRows - 1) / kRows;
+    p.units = B * Hkv * p.RB;
+    p.F = p.RB == 1 ? replicas_of(p.M) : 1;
+    p.max_steps = static_cast<long long>(p.units) *
+                  chunks_of(static_cast<int>(static_cast<long long>(max_pages) * P > (1LL << 30)
+                                                 ? (1LL << 30)
+                                                 : static_cast<long long>(max_pages) * P));
+    if (n_ctas_req > 0) {
+        p.n_ctas = n_ctas_req;
+    } else {
+        const long long cap = p.max_steps > 0 ? p.max_steps : 1;
+        p.n_ctas = sm_count < cap ? sm_count : static_cast<int>(cap);
+    }
+    const long long units = p.units > 0 ? p.units : 1;
+    const long long expect = (p.n_ctas / units + 2) * p.F;
+    p.merge_wpr = expect > 12 ? 4 : (expect > 6 ? 2 : 1);
+    return p;
+}
+
 }  // namespace treeattn

@@ -84,7 +84,13 @@ int check_common(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pa
     return TREE_ATTN_OK;
 }
 
-int resolve_ctas(int n_ctas) { return n_ctas > 0 ? n_ctas : sm_count(); }
+// CTAs of the prefix pass: the caller's count, else the kernel selector's.
+int resolve_ctas(int n_ctas, int B, int Hq, int Hkv, int T, int P, int max_pages) {
+    if (n_ctas > 0) return n_ctas;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    return make_plan(B, Hq, Hkv, T, P, max_pages, sms, 0).n_ctas;
+}
 
 float to_log2(float softmax_scale) {
     return static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
@@ -133,6 +139,24 @@ size_t tree_attn_workspace_size_ctas(int B, int Hq, int Hkv, int d, int T, int p
     return ws_bytes(B, Hq, Hkv, d, T, n_ctas);
 }
 
+int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pages_per_seq,
+                   int sm_count_hint, tree_attn_plan_info* out) {
+    if (out == nullptr) return TREE_ATTN_ERR_NULL;
+    if (!shape_ok(B, Hq, Hkv, d, T, page_size) || max_pages_per_seq < 1)
+        return TREE_ATTN_ERR_SHAPE;
+    const int sms = sm_count_hint > 0 ? sm_count_hint : sm_count();
+    if (sms <= 0) return TREE_ATTN_ERR_CUDA;
+    const Plan p = make_plan(B, Hq, Hkv, T, page_size, max_pages_per_seq, sms, 0);
+    out->units = p.units;
+    out->row_blocks = p.RB;
+    out->replicas = p.F;
+    out->n_ctas = p.n_ctas;
+    out->merge_warps_per_row = p.merge_wpr;
+    out->max_steps = p.max_steps;
+    out->workspace_bytes = ws_bytes(B, Hq, Hkv, d, T, p.n_ctas);
+    return TREE_ATTN_OK;
+}
+
 size_t tree_attn_workspace_size(int B, int Hq, int Hkv, int d, int T, int max_seq_len,
                                 int page_size) {
     (void)max_seq_len;
@@ -153,7 +177,7 @@ int tree_attn_prefix_pass(const uint16_t* q, const uint16_t* k_pages, const uint
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
         !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(status, 4))
         return TREE_ATTN_ERR_ALIGN;
-    n_ctas = resolve_ctas(n_ctas);
+    n_ctas = resolve_ctas(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq);
     if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
@@ -191,7 +215,7 @@ int tree_attn_suffix_merge(const uint16_t* q, const int32_t* seq_lens, int max_p
     if (!aligned(q, 16) || !aligned(tree_k, 16) || !aligned(tree_v, 16) || !aligned(out, 16) ||
         !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8))
         return TREE_ATTN_ERR_ALIGN;
-    n_ctas = resolve_ctas(n_ctas);
+    n_ctas = resolve_ctas(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq);
     if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
@@ -255,7 +279,7 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
         !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8) || !aligned(status, 4))
         return TREE_ATTN_ERR_ALIGN;
-    n_ctas = resolve_ctas(n_ctas);
+    n_ctas = resolve_ctas(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq);
     if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))

@@ -1,0 +1,82 @@
+"""The kernel selector (tree_attn_plan): the launch choices for each workload
+shape, computed on the host only (CPU)."""
+import pytest
+
+import speculative_decoding_tree_split_gb300 as ta
+from workloads import CONFIGS
+
+SMS = 152   # GB300
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ta.build()
+    ta.load()
+
+
+def max_pages(cfg):
+    hi = cfg.L[1] if isinstance(cfg.L, tuple) else cfg.L
+    return (hi + cfg.page - 1) // cfg.page
+
+
+# (units, row blocks, replicas, CTAs, merge warps per row), worked out by hand:
+#   units = B * Hkv * ceil(T*G/128); replicas 4 for M <= 32, 2 for M <= 64;
+#   CTAs = min(152, units * ceil(max_pages*P/64));
+#   merge warps from (CTAs // units + 2) * replicas: > 12 -> 4, > 6 -> 2, else 1.
+EXPECTED = {
+    "tiny": (2, 1, 4, 4, 4),          # M = 16; 2 units x 2 steps = 4 CTAs; (2+2)*4 = 16
+    "llama8b": (8, 1, 2, 152, 4),     # M = 48; (19+2)*2 = 42
+}
+
+def test_plan_llama8b_and_tiny_by_hand():
+    for name in ("tiny", "llama8b"):
+        c = CONFIGS[name]
+        p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+        got = (p["units"], p["row_blocks"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"])
+        assert got == EXPECTED[name], (name, got)
+
+
+def test_plan_other_workloads_by_hand():
+    # llama70b: M = 8 * 8 = 64 -> 2 replicas; units 16*8 = 128; 152 // 128 = 1 -> (1+2)*2 = 6
+    c = CONFIGS["llama70b"]
+    p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+    assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (128, 2, 152, 1)
+    # chain: M = 4 * 4 = 16 -> 4 replicas; units 512; (0+2)*4 = 8 -> 2 warps
+    c = CONFIGS["chain"]
+    p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+    assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (512, 4, 152, 2)
+    # maverick: M = 16 * 5 = 80 -> 1 copy; units 32; (4+2)*1 = 6 -> 1 warp
+    c = CONFIGS["maverick"]
+    p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+    assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (32, 1, 152, 1)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,T,P,maxp", [
+    (1, 8, 8, 64, 1, 16, 1), (3, 16, 4, 128, 10, 64, 11), (1, 8, 2, 128, 64, 64, 5),
+    (64, 64, 8, 128, 64, 128, 200), (2, 40, 8, 128, 16, 32, 4), (1, 128, 1, 128, 64, 16, 1)])
+def test_plan_invariants(B, Hq, Hkv, d, T, P, maxp):
+    p = ta.plan(B, Hq, Hkv, d, T, P, maxp, SMS)
+    G = Hq // Hkv
+    M = T * G
+    assert p["row_blocks"] == (M + 127) // 128
+    assert p["units"] == B * Hkv * p["row_blocks"]
+    assert p["max_steps"] == p["units"] * ((maxp * P + 63) // 64)
+    assert 1 <= p["n_ctas"] <= min(SMS, max(1, p["max_steps"]))
+    if p["row_blocks"] == 1:
+        assert p["replicas"] * M <= 128 or p["replicas"] == 1
+        assert p["replicas"] in (1, 2, 4)
+    else:
+        assert p["replicas"] == 1
+    assert p["merge_warps_per_row"] in (1, 2, 4)
+    lib = ta.load()
+    assert p["workspace_bytes"] == lib.tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, P,
+                                                                      p["n_ctas"])
+    # the selector never needs more scratch than the size callers allocate by
+    assert p["workspace_bytes"] <= lib.tree_attn_workspace_size_ctas(B, Hq, Hkv, d, T, P, SMS)
+
+
+def test_plan_rejects_bad_shapes():
+    with pytest.raises(ta.TreeAttnError):
+        ta.plan(1, 6, 4, 128, 4, 64, 4, SMS)
+    with pytest.raises(ta.TreeAttnError):
+        ta.plan(1, 8, 2, 128, 4, 64, 0, SMS)
