@@ -2,10 +2,12 @@
 """Benchmark of split tree attention (verification attention of tree
 speculative decoding) on one or more GPUs of one node.
 
-A step is one pass of the whole hot path over one batch: tree_mask_build
-(ancestor bitmasks of the draft tree) followed by tree_attn_verify (prefix
-pass split over the paged KV cache, tree-masked suffix pass, log-sum-exp
-merge), through the C ABI.
+A step is one pass of the whole hot path over one batch through the C ABI:
+the ancestor bitmasks of the draft tree, the prefix pass split over the paged
+KV cache, the tree-masked suffix pass and the log-sum-exp merge.  With the
+default layout it is one tree_attn_verify_tree call (the masks are built
+inside the suffix/merge kernel); --layout paged_tree / full_mask call
+tree_mask_build first.
 
     python bench.py [--config llama8b] [--steps K] [--warmup W]
     python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
@@ -39,6 +41,8 @@ if _ROOT not in sys.path:
 from workloads import CONFIGS, make_workload  # noqa: E402
 
 METRIC = "verified tree tokens/s per layer"
+# kernels one step launches, per layout
+LAUNCHES_PER_STEP = {"shared": 2, "per_seq": 2, "paged_tree": 3, "full_mask": 4}
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -345,17 +349,18 @@ def run_ours(args):
             ta.verify_dense(q_, k_, v_, bt_, key_lens, dense, out=out, lse=lse, workspace=ws,
                             status=status, softmax_scale=wl.scale)
         elif layout == "per_seq":
-            ta.mask_build_batched(par, mask_out=mask, status=status)
-            ta.verify_batched(q_, k_, v_, bt_, sl_, tk_, tv_, mask, out=out, lse=lse,
-                              workspace=ws, status=status, softmax_scale=wl.scale)
+            # the masks are built inside the verify call (tree_attn_verify_tree)
+            ta.verify_tree(q_, k_, v_, bt_, sl_, tk_, tv_, par, mask_out=mask, out=out, lse=lse,
+                           workspace=ws, status=status, softmax_scale=wl.scale)
         elif layout == "paged_tree":
             ta.mask_build(par, mask_out=mask, status=status)
             ta.verify_paged_tree(q_, k_, v_, bt_, sl_, mask, out=out, lse=lse, workspace=ws,
                                  status=status, softmax_scale=wl.scale)
         else:
-            ta.mask_build(par, mask_out=mask, status=status)
-            ta.verify(q_, k_, v_, bt_, sl_, tk_, tv_, mask, out=out, lse=lse, workspace=ws,
-                      status=status, softmax_scale=wl.scale)
+            # tree_mask_build + tree_attn_verify in one call: the ancestor
+            # masks are built inside the suffix/merge kernel and written out
+            ta.verify_tree(q_, k_, v_, bt_, sl_, tk_, tv_, par, mask_out=mask, out=out, lse=lse,
+                           workspace=ws, status=status, softmax_scale=wl.scale)
 
     def step(r):
         hot_path(parents, q, kps[r % R], vps[r % R], bt, sl, tk, tv)
@@ -504,7 +509,7 @@ def run_ours(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes["prefix_kernel"],
                          "peak_source": peak_src, "kernel_sha": sha},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * K,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP[layout] * K,
             "cpu_baseline": cpu,
         })
     if world > 1:

@@ -189,6 +189,31 @@ TREE_ATTN_API int tree_attn_verify_batched(const uint16_t *q, const uint16_t *k_
                                            size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * tree_attn_verify_tree -- tree_mask_build and tree_attn_verify in one call:
+ * the ancestor masks are built inside the suffix/merge kernel from the
+ * parent array (one warp's pointer jumping per row, the same algorithm as
+ * tree_mask_build), which removes a kernel and its dependency hop from the
+ * step.
+ *
+ *   parents         int32 [T] (parents_stride 0, one tree) or [B][T]
+ *                   (parents_stride T, one tree per sequence)
+ *   mask_out        nullable uint64 [T] / [B][T]: the masks, for later use
+ *                   (e.g. tree_greedy_accept)
+ *   status          also receives TREE_ATTN_STATUS_BAD_PARENT
+ *
+ * Everything else as tree_attn_verify.
+ */
+TREE_ATTN_API int tree_attn_verify_tree(const uint16_t *q, const uint16_t *k_pages,
+                                        const uint16_t *v_pages, const int32_t *block_table,
+                                        int max_pages_per_seq, const int32_t *seq_lens,
+                                        const uint16_t *tree_k, const uint16_t *tree_v,
+                                        const int32_t *parents, int parents_stride,
+                                        uint64_t *mask_out, uint16_t *out, float *lse, int B,
+                                        int Hq, int Hkv, int d, int T, int page_size,
+                                        int num_pages, float softmax_scale, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
  * tree_attn_verify_paged_tree -- split tree attention with the draft tokens
  * padded into the paged KV cache ("paged KV with tree padding", pith.science
  * verdict record, desk editor's note): tree token j of sequence b has its

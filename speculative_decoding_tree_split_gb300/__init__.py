@@ -29,6 +29,7 @@ from ._lib import (  # noqa: F401
     verify,
     verify_batched,
     verify_paged_tree,
+    verify_tree,
     greedy_accept,
     dense_cols_for,
     dense_mask_build,

@@ -52,6 +52,7 @@ EXPORTED = (
     "tree_dense_mask_build",
     "tree_attn_verify_dense",
     "tree_attn_plan",
+    "tree_attn_verify_tree",
 )
 
 
@@ -125,6 +126,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                    ctypes.POINTER(PlanInfo)]
     lib.tree_attn_plan.restype = i32
+    lib.tree_attn_verify_tree.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp,
+                                          i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
+    lib.tree_attn_verify_tree.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -266,6 +270,43 @@ def verify_batched(q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, m
     return _verify_generic("tree_attn_verify_batched", q, k_pages, v_pages, block_table,
                            seq_lens, tree_k, tree_v, masks, out, lse, workspace, status,
                            softmax_scale, stream)
+
+
+def verify_tree(q, k_pages, v_pages, block_table, seq_lens, tree_k, tree_v, parents, *,
+                mask_out=None, out=None, lse=None, workspace=None, status=None,
+                softmax_scale=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Mask build + split tree attention in one call: parents int32 [T] or
+    [B][T]; the masks are built on the device (and written to mask_out if
+    given)."""
+    bf = (torch.bfloat16,)
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (tree_k, "tree_k"),
+                 (tree_v, "tree_v")):
+        _check(t, n, bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    _check(parents, "parents", (torch.int32,))
+    if mask_out is not None:
+        _check(mask_out, "mask_out", _BITS64)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    stride = T if parents.dim() == 2 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = workspace_size(B, Hq, Hkv, d, T, 0, P)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = load().tree_attn_verify_tree(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), _ptr(tree_k), _ptr(tree_v), _ptr(parents), stride, _ptr(mask_out),
+        _ptr(out), _ptr(lse), B, Hq, Hkv, d, T, P, num_pages, float(softmax_scale),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_attn_verify_tree", rc)
+    return out, lse
 
 
 def verify_paged_tree(q, k_pages, v_pages, block_table, seq_lens, mask, *, out=None, lse=None,

@@ -57,19 +57,12 @@ __device__ __forceinline__ int pick32(int lo, int hi, int node) {
     return node < 32 ? a : b;
 }
 
-__global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
-                                                       uint64_t* __restrict__ mask,
-                                                       int32_t* status) {
-    // CTA b builds the mask of tree b (a batch of trees is [B][T]).
-    parents += static_cast<size_t>(blockIdx.x) * T;
-    mask += static_cast<size_t>(blockIdx.x) * T;
-    // The next kernel may start its prologue now; it waits for this grid
-    // before reading anything this grid writes.
-    ptx::grid_dep_launch();
-    ptx::grid_dep_wait();
-    const int lane = threadIdx.x;
+// Ancestor-or-self masks of one tree (T <= 64 nodes, parents[i] in [-1, i)),
+// computed by one warp: lane l returns the masks of nodes l and l + 32.
+// Returns true if a parent was invalid (that node is then taken as a root).
+__device__ __forceinline__ bool warp_tree_mask(const int32_t* parents, int T, int lane,
+                                               uint64_t anc[2]) {
     int jump[2];
-    uint64_t anc[2];
     bool bad = false;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -85,7 +78,6 @@ __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict
         jump[h] = p;
         anc[h] = (i < T) ? (1ull << i) : 0ull;
     }
-    if (__any_sync(kFull, bad) && lane == 0) report(status, TREE_ATTN_STATUS_BAD_PARENT);
 #pragma unroll
     for (int round = 0; round < 6; ++round) {
         uint64_t na[2];
@@ -104,6 +96,23 @@ __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict
             jump[h] = nj[h];
         }
     }
+    return __any_sync(kFull, bad);
+}
+
+__global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
+                                                       uint64_t* __restrict__ mask,
+                                                       int32_t* status) {
+    // CTA b builds the mask of tree b (a batch of trees is [B][T]).
+    parents += static_cast<size_t>(blockIdx.x) * T;
+    mask += static_cast<size_t>(blockIdx.x) * T;
+    // The next kernel may start its prologue now; it waits for this grid
+    // before reading anything this grid writes.
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    const int lane = threadIdx.x;
+    uint64_t anc[2];
+    if (warp_tree_mask(parents, T, lane, anc) && lane == 0)
+        report(status, TREE_ATTN_STATUS_BAD_PARENT);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int i = lane + 32 * h;
@@ -818,6 +827,12 @@ struct MergeArgs {
     const int32_t* block_table;
     int num_pages;
     int32_t* status;
+    // Tree masks built here from parent arrays (mask == nullptr then):
+    // parents [T] (parents_stride 0) or [B][T] (parents_stride T); the masks
+    // are also written to mask_out when it is not null.
+    const int32_t* parents;
+    int parents_stride;
+    uint64_t* mask_out;
 };
 
 template <int E>
@@ -931,11 +946,33 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    if (active && sub == 0 && a.mask != nullptr) {
+    // Tree mask of this row's node: given, or built here from the parent
+    // array (one warp's pointer jumping, as in tree_mask_kernel).
+    uint64_t bits = 0;
+    if (a.parents != nullptr && sub == 0) {
+        uint64_t anc[2];
+        const bool bad_tree = warp_tree_mask(
+            a.parents + static_cast<size_t>(b) * a.parents_stride, a.T, lane, anc);
+        bits = pick64(anc[0], anc[1], t);
+        // One warp per tree reports and writes the masks out: the first
+        // unit's of the sequence (per-sequence trees) or of the batch.
+        const bool writer = unit == b * upb && blockIdx.y == 0 && warp == 0 &&
+                            (a.parents_stride != 0 || b == 0);
+        if (writer && bad_tree && lane == 0) report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
+        if (writer && a.mask_out != nullptr) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = lane + 32 * hh;
+                if (i < a.T) a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
+            }
+        }
+    } else if (a.mask != nullptr && active && sub == 0) {
+        bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
+    }
+    if (a.T < 64) bits &= (1ull << a.T) - 1ull;
+    if (active && sub == 0 && (a.mask != nullptr || a.parents != nullptr)) {
         float qv[E];
         load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
-        uint64_t bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
-        if (a.T < 64) bits &= (1ull << a.T) - 1ull;
         int L_b = 0;
         if (a.tree_in_cache) {
             bool bad_len;
@@ -1240,6 +1277,9 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.block_table = v.block_table;
     ma.num_pages = v.num_pages;
     ma.status = v.status;
+    ma.parents = v.parents;
+    ma.parents_stride = v.parents_stride;
+    ma.mask_out = v.mask_out;
     const Plan plan = make_plan(v.B, v.Hq, v.Hkv, v.T, v.P, v.max_pages, v.n_ctas, v.n_ctas);
     const long long units = plan.units;
     const int F = plan.F;

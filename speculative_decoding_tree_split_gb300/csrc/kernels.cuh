@@ -31,6 +31,12 @@ struct VerifyArgs {
     // (mask == nullptr).  nullptr: the split form.
     const uint8_t* dense;
     int dense_cols;
+    // Masks built by the merge kernel from parent arrays ([T] or [B][T],
+    // parents_stride 0 or T) instead of read from `mask`; written to
+    // mask_out when it is not null.
+    const int32_t* parents;
+    int parents_stride;
+    uint64_t* mask_out;
 };
 
 // Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and

@@ -255,11 +255,19 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
                   int mask_stride, bool tree_in_cache, uint16_t* out, float* lse, int B, int Hq,
                   int Hkv, int d, int T, int page_size, int num_pages, float softmax_scale,
                   void* workspace, size_t workspace_bytes, int32_t* status, void* stream,
-                  int n_ctas, const uint8_t* dense = nullptr, int dense_cols = 0) {
+                  int n_ctas, const uint8_t* dense = nullptr, int dense_cols = 0,
+                  const int32_t* parents = nullptr, int parents_stride = 0,
+                  uint64_t* mask_out = nullptr) {
     if (mask_stride != 0 && mask_stride != T) return TREE_ATTN_ERR_SHAPE;
     if (tree_in_cache) {
         tree_k = k_pages;  // unused: keep the null checks below meaningful
         tree_v = v_pages;
+    }
+    if (parents != nullptr) {
+        // Masks built inside the merge kernel from the parent arrays.
+        if (parents_stride != 0 && parents_stride != T) return TREE_ATTN_ERR_SHAPE;
+        if (!aligned(parents, 4) || !aligned(mask_out, 8)) return TREE_ATTN_ERR_ALIGN;
+        mask = reinterpret_cast<const uint64_t*>(parents);  // non-null for the checks below
     }
     if (dense != nullptr) {
         // One pass under the explicit mask: no tree mask, no suffix.
@@ -313,6 +321,10 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
     a.dense = dense;
     a.dense_cols = dense_cols;
     if (dense != nullptr) a.mask = nullptr;
+    a.parents = parents;
+    a.parents_stride = parents_stride;
+    a.mask_out = mask_out;
+    if (parents != nullptr) a.mask = nullptr;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = prefix_impl(a, k_pages, v_pages, st);
     if (rc != TREE_ATTN_OK) return rc;
@@ -360,6 +372,21 @@ int tree_attn_verify_paged_tree(const uint16_t* q, const uint16_t* k_pages,
                          nullptr, mask, mask_stride, true, out, lse, B, Hq, Hkv, d, T,
                          page_size, num_pages, softmax_scale, workspace, workspace_bytes, status,
                          stream, 0);
+}
+
+int tree_attn_verify_tree(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                          const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, const uint16_t* tree_k,
+                          const uint16_t* tree_v, const int32_t* parents, int parents_stride,
+                          uint64_t* mask_out, uint16_t* out, float* lse, int B, int Hq, int Hkv,
+                          int d, int T, int page_size, int num_pages, float softmax_scale,
+                          void* workspace, size_t workspace_bytes, int32_t* status,
+                          void* stream) {
+    if (parents == nullptr) return TREE_ATTN_ERR_NULL;
+    return verify_common(q, k_pages, v_pages, block_table, max_pages_per_seq, seq_lens, tree_k,
+                         tree_v, nullptr, 0, false, out, lse, B, Hq, Hkv, d, T, page_size,
+                         num_pages, softmax_scale, workspace, workspace_bytes, status, stream, 0,
+                         nullptr, 0, parents, parents_stride, mask_out);
 }
 
 int tree_dense_mask_build(const uint64_t* mask, int mask_stride, const int32_t* seq_lens, int B,

@@ -214,3 +214,22 @@ def test_dense_entries_host_checks(lib):
     args = list(base)
     args[6] = a + 4
     assert v(*args) == -3
+
+
+def test_verify_tree_host_checks(lib):
+    a = A16
+    f = lib.tree_attn_verify_tree
+    base = [a, a, a, a, 4, a, a, a, a, 0, None, a, a, 2, 8, 2, 128, 4, 64, 8, 0.1, a, 1 << 30,
+            None, None]
+    args = list(base)
+    args[8] = None
+    assert f(*args) == -1          # parents
+    args = list(base)
+    args[9] = 3
+    assert f(*args) == -2          # stride neither 0 nor T
+    args = list(base)
+    args[8] = a + 2
+    assert f(*args) == -3
+    args = list(base)
+    args[10] = a + 4
+    assert f(*args) == -3          # mask_out alignment

@@ -292,3 +292,60 @@ def test_row_replication_paths(oracle, T, G, n_ctas):
     cfg = Config(f"rep{T}x{G}", B=2, Hq=2 * G, Hkv=2, d=128, L=(0, 1000), page=64, T=T,
                  max_depth=5, max_branch=4, seed=40 + T)
     compare_all(oracle, make_workload(cfg, seq_lens=[997, 650]), n_ctas=n_ctas)
+
+
+# ---------------------------------------------------------------------------
+# masks built inside the merge kernel (tree_attn_verify_tree)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("per_seq", [False, True], ids=["shared", "per_seq"])
+def test_verify_tree_equals_mask_build_then_verify(oracle, per_seq):
+    cfg = Config("vt", B=3, Hq=32, Hkv=8, d=128, L=(0, 3000), page=64, T=12, seed=91)
+    wl = make_workload(cfg, seq_lens=[3000, 0, 1031], per_sequence_trees=per_seq)
+    x = to_dev(wl)
+    if per_seq:
+        mask = ta.mask_build_batched(x["parents"])
+        o1, l1 = ta.verify_batched(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                                   x["seq_lens"], x["tree_k"], x["tree_v"], mask,
+                                   softmax_scale=wl.scale)
+    else:
+        mask = ta.mask_build(x["parents"])
+        o1, l1 = ta.verify(x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["seq_lens"],
+                           x["tree_k"], x["tree_v"], mask, softmax_scale=wl.scale)
+    mask_out = torch.zeros_like(mask)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o2, l2 = ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                            x["seq_lens"], x["tree_k"], x["tree_v"], x["parents"],
+                            mask_out=mask_out, status=status, softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(mask_out, mask)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if not per_seq:
+        ref_o, ref_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
+        assert np.abs(o2.float().cpu().numpy() - ref_o).max() <= OUT_TOL
+        assert np.abs(l2.cpu().numpy() - ref_l).max() <= LSE_TOL
+
+
+def test_verify_tree_bad_parent_sets_status():
+    cfg = Config("vb", B=2, Hq=8, Hkv=2, d=128, L=(0, 300), page=64, T=4, seed=92)
+    wl = make_workload(cfg, seq_lens=[200, 100], parents=torch.tensor([-1, 0, 3, 1]))
+    x = to_dev(wl)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["seq_lens"],
+                   x["tree_k"], x["tree_v"], x["parents"], status=status,
+                   softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == ta.STATUS_BAD_PARENT
+
+
+@pytest.mark.parametrize("n_ctas", [2, 19, 152])
+def test_many_partials_per_row(oracle, n_ctas):
+    # one long sequence, few units: rows collect up to ~80 partials, which
+    # exercises the merge's batches past the first round trip
+    cfg = Config("mp", B=1, Hq=16, Hkv=2, d=128, L=(0, 12000), page=64, T=4, seed=93)
+    wl = make_workload(cfg, seq_lens=[11997])
+    mask, out, lse, status = run_gpu(wl, n_ctas=n_ctas)
+    assert status == 0
+    ref_o, ref_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
+    assert np.abs(out - ref_o).max() <= OUT_TOL
+    assert np.abs(lse - ref_l).max() <= LSE_TOL
