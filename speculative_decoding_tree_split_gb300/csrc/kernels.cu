@@ -250,6 +250,11 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     }
 }
 
+// Barrier among `count` threads (whole warps) on hardware barrier `id`.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -756,10 +761,88 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             ptx::tc_fence_after();
-            if (warp_any) {
-                float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
-                const uint32_t to = lane_base + S::TM_O;
-                const float acc_scale = (DENSE && l_rnd > 0.f) ? l_sum / l_rnd : 1.f;
+            float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
+            const uint32_t to = lane_base + S::TM_O;
+            const float acc_scale = (DENSE && l_rnd > 0.f) ? l_sum / l_rnd : 1.f;
+            if (F > 1 && !have_next) {
+                // Last segment of this CTA: every MMA and copy has completed,
+                // so the K/V ring is free.  Fold the F row copies into copy 0
+                // through it (rows padded to D + 4 floats, conflict-free), so
+                // the merge reads one partial per CTA instead of F.
+                constexpr int RS = D + 4;
+                float* stg = reinterpret_cast<float*>(smem + S::OFF_STAGE);  // [F-1][R][RS]
+                float* stg_ml = stg + (F - 1) * R * RS;                       // [F-1][R][2]
+                if (g >= 1 && warp_any) {
+                    float* dst = stg + static_cast<size_t>((g - 1) * R + lr) * RS;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        ptx::tmem_ld32(to + c, o);
+                        ptx::tmem_wait_ld();
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                *reinterpret_cast<float4*>(dst + c + 4 * i) =
+                                    make_float4(o[4 * i] * acc_scale, o[4 * i + 1] * acc_scale,
+                                                o[4 * i + 2] * acc_scale, o[4 * i + 3] * acc_scale);
+                        }
+                    }
+                    if (row_ok) {
+                        stg_ml[((g - 1) * R + lr) * 2] = m_ref;
+                        stg_ml[((g - 1) * R + lr) * 2 + 1] = l_sum;
+                    }
+                }
+                named_bar_sync(1, 128);
+                if (g == 0 && warp_any) {
+                    float mg[F], wg[F];
+                    mg[0] = m_ref;
+                    float mx = m_ref, lc = 0.f;
+#pragma unroll
+                    for (int k = 1; k < F; ++k) {
+                        mg[k] = row_ok ? stg_ml[((k - 1) * R + lr) * 2] : kNegInf;
+                        mx = fmaxf(mx, mg[k]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < F; ++k) {
+                        wg[k] = (mg[k] == kNegInf) ? 0.f : ptx::ex2(mg[k] - mx);
+                        lc += wg[k] * (k == 0 ? l_sum
+                                              : (row_ok ? stg_ml[((k - 1) * R + lr) * 2 + 1] : 0.f));
+                    }
+                    float4* acc =
+                        reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        ptx::tmem_ld32(to + c, o);
+                        ptx::tmem_wait_ld();
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= wg[0] * acc_scale;
+#pragma unroll
+                            for (int k = 1; k < F; ++k) {
+                                const float* src =
+                                    stg + static_cast<size_t>((k - 1) * R + lr) * RS + c;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float4 x = *reinterpret_cast<const float4*>(src + 4 * i);
+                                    o[4 * i] = fmaf(wg[k], x.x, o[4 * i]);
+                                    o[4 * i + 1] = fmaf(wg[k], x.y, o[4 * i + 1]);
+                                    o[4 * i + 2] = fmaf(wg[k], x.z, o[4 * i + 2]);
+                                    o[4 * i + 3] = fmaf(wg[k], x.w, o[4 * i + 3]);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[c / 4 + i] =
+                                    make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                        }
+                    }
+                    if (row_ok) {
+                        slot[r] = mx;
+                        slot[kRows + r] = lc;
+                    }
+                }
+            } else if (warp_any) {
                 float4* acc =
                     reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
 #pragma unroll
@@ -884,7 +967,7 @@ constexpr int kMergeWarps = 4;  // warps per CTA
 // memory.  Every independent load of a phase is issued before any of its
 // results is used, so each phase costs about one memory round trip.
 template <int D, int F>
-__global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const MergeArgs a) {
     constexpr int E = D / 32;
     constexpr int R = kRows / F;
     const int warp = threadIdx.x >> 5;
@@ -933,10 +1016,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     bool bad;
     const int nch = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
     int c_first = 0, c_last = -1;
+    // A prefix CTA folds its F row copies into one partial in its last
+    // segment.  Every CTA before c_last ends inside this unit; c_last does
+    // only if its range stops at the unit's end.
+    bool last_folded = F == 1;
     if (nch > 0) {
         const long long ustart = base_b + static_cast<long long>(unit - b * upb) * nch;
         c_first = cta_of(ustart, W, a.n_ctas);
         c_last = cta_of(ustart + nch - 1, W, a.n_ctas);
+        if (F > 1) last_folded = cta_start(c_last + 1, W, a.n_ctas) <= ustart + nch;
     }
 
     // ---- suffix (sub-warp 0 of each row): softmax over the tree keys
@@ -1062,24 +1150,28 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 8) suffix_merge_kernel(const
     // ---- merge with the partials of the prefix pass
     ptx::grid_dep_wait();
     const size_t sf = static_cast<size_t>(slot_floats(D));
-    // Partials are indexed by "virtual slot" v: prefix CTA c = c_first + v / F
-    // and query-row copy g = v % F of that CTA's tile (rows g * R + r).  This
+    // Partials are indexed by "virtual slot" v: v < n1 is the folded partial
+    // of prefix CTA c_first + v (copy 0, tile rows r); the rest are those of
+    // c_last: one if it folded, else its F copies (tile rows g * R + r).  This
     // warp takes v = sub, sub + wpr, ...; its k-th one is v = sub + k * wpr.
-    const int nv = active ? (c_last - c_first + 1) * F : 0;
+    const int n1 = c_last - c_first;
+    const int nv = (active && nch > 0) ? n1 + (last_folded ? 1 : F) : 0;
+    auto v_cta = [&](int v) -> int { return v < n1 ? c_first + v : c_last; };
+    auto v_copy = [&](int v) -> int { return v < n1 ? 0 : v - n1; };
     const int nmine = nv > sub ? (nv - sub + wpr - 1) / wpr : 0;
     // With at least one work-line step per CTA every CTA in [c_first, c_last]
     // wrote a partial; only when W < C can some of them be empty.
     const bool every_cta = W >= a.n_ctas;
     auto v_of = [&](int k) -> int { return sub + k * wpr; };
     auto v_m = [&](int v) -> size_t {  // offset of m for virtual slot v
-        return static_cast<size_t>(unit + c_first + v / F) * sf + (v % F) * R + r;
+        return static_cast<size_t>(unit + v_cta(v)) * sf + v_copy(v) * R + r;
     };
     auto v_acc = [&](int v) -> size_t {  // offset of this lane's accumulator values
-        return static_cast<size_t>(unit + c_first + v / F) * sf + 2 * kRows +
-               static_cast<size_t>((v % F) * R + r) * D + lane * E;
+        return static_cast<size_t>(unit + v_cta(v)) * sf + 2 * kRows +
+               static_cast<size_t>(v_copy(v) * R + r) * D + lane * E;
     };
     auto v_work = [&](int v) -> bool {
-        return every_cta || cta_has_work(c_first + v / F, W, a.n_ctas);
+        return every_cta || cta_has_work(v_cta(v), W, a.n_ctas);
     };
     // One round trip: (m, l) of this warp's first 32 partials (lane k: the
     // k-th) and the accumulator rows of its first four.  Partials are read

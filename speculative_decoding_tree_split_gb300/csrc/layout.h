@@ -217,7 +217,8 @@ TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>
 //   F          query-row copies per tile when one 128-row block holds the
 //              unit's rows (small M: the softmax work per CTA is split);
 //   merge_wpr  warps per query row in the merge, from the partials a row
-//              expects: prefix CTAs per unit (+2 for straddled ends) x F.
+//              expects: prefix CTAs per unit, +1 for a straddled end, +F
+//              for the unfolded copies of the last CTA.
 struct Plan {
     int G, M, RB, units, F, n_ctas, merge_wpr;
     long long max_steps;
@@ -242,7 +243,9 @@ TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm
         p.n_ctas = sm_count < cap ? sm_count : static_cast<int>(cap);
     }
     const long long units = p.units > 0 ? p.units : 1;
-    const long long expect = (p.n_ctas / units + 2) * p.F;
+    // Prefix CTAs fold their F row copies in their last segment, so a row
+    // sees about one partial per CTA plus the F copies of a straddling CTA.
+    const long long expect = p.n_ctas / units + 1 + p.F;
     p.merge_wpr = expect > 12 ? 4 : (expect > 6 ? 2 : 1);
     return p;
 }

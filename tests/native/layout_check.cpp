@@ -3,12 +3,17 @@
 //   * partial-result slots (unit + cta) are unique and < units + CTAs,
 //   * the merge side's slot range for a unit (cta_of of the unit's first and
 //     last work-line positions) names exactly the CTAs that wrote it,
+//   * with F query-row copies per tile, the partials the merge enumerates
+//     (one folded partial per CTA before the unit's last CTA, then the last
+//     CTA's one folded or F unfolded copies) are exactly those written: a
+//     prefix CTA folds its copies in its last segment only,
 //   * the descriptor helpers put each field where the bit layout says.
 // Prints "OK" and exits 0, or prints the first failure and exits 1.
 #include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <set>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -32,9 +37,10 @@ static unsigned next_rand() {
         }                                                    \
     } while (0)
 
-static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C,
+static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int F,
                             const std::vector<int32_t>& sl) {
     const int upb = Hkv * RB;
+    std::set<std::tuple<int, int, int>> parts;  // (unit, CTA, copy) written
     std::map<std::pair<int, int>, int> covered;  // (unit, chunk) -> count
     std::map<int, std::set<int>> writers;        // unit -> CTAs
     std::set<long long> slots;
@@ -47,7 +53,9 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C,
         w.init(sl.data(), B, P, maxp, upb, RB, b0, base0, x0, x1);
         Segment s;
         long long done = 0;
+        std::vector<Segment> segs;
         while (w.next(s)) {
+            segs.push_back(s);
             CHECK(s.chunk_end > s.chunk_begin, "empty segment");
             CHECK(s.unit == (s.b * Hkv + s.hk) * RB + s.rb, "unit index");
             bool bad;
@@ -61,6 +69,11 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C,
             done += s.chunk_end - s.chunk_begin;
         }
         CHECK(done == x1 - x0, "CTA range not fully walked");
+        for (size_t k = 0; k < segs.size(); ++k) {
+            const bool fold = F > 1 && k + 1 == segs.size();
+            for (int g = 0; g < (fold ? 1 : F); ++g)
+                parts.insert(std::make_tuple(segs[k].unit, c, g));
+        }
     }
     long long base = 0;
     for (int b = 0; b < B; ++b) {
@@ -80,6 +93,23 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C,
                     if (cta_has_work(c, W, C)) want.insert(c);
             }
             CHECK(want == writers[unit], "merge-side CTA range mismatch for unit %d", unit);
+            // the merge's enumeration of this unit's partials
+            std::set<std::tuple<int, int, int>> got, have;
+            for (const auto& t : parts)
+                if (std::get<0>(t) == unit) have.insert(t);
+            if (nch > 0) {
+                const long long us = base + static_cast<long long>(urel) * nch;
+                const int cf = cta_of(us, W, C), cl = cta_of(us + nch - 1, W, C);
+                const bool last_folded = F == 1 || cta_start(cl + 1, W, C) <= us + nch;
+                const int n1 = cl - cf;
+                const int nv = n1 + (last_folded ? 1 : F);
+                for (int v = 0; v < nv; ++v) {
+                    const int cta = v < n1 ? cf + v : cl;
+                    const int copy = v < n1 ? 0 : v - n1;
+                    if (cta_has_work(cta, W, C)) got.insert(std::make_tuple(unit, cta, copy));
+                }
+            }
+            CHECK(got == have, "merge-side partial list mismatch for unit %d (F=%d)", unit, F);
         }
         base += static_cast<long long>(upb) * nch;
     }
@@ -131,10 +161,12 @@ int main() {
             else
                 sl[b] = next_rand() % (maxp * P + 1);
         }
-        if (!check_partition(B, Hkv, RB, P, maxp, C, sl)) {
-            std::printf("  at trial %d (B=%d Hkv=%d RB=%d P=%d maxp=%d C=%d)\n", trial, B, Hkv,
-                        RB, P, maxp, C);
-            return 1;
+        for (int F = 1; F <= (RB == 1 ? 4 : 1); F *= 2) {
+            if (!check_partition(B, Hkv, RB, P, maxp, C, F, sl)) {
+                std::printf("  at trial %d (B=%d Hkv=%d RB=%d P=%d maxp=%d C=%d F=%d)\n", trial,
+                            B, Hkv, RB, P, maxp, C, F);
+                return 1;
+            }
         }
     }
     std::printf("OK\n");

@@ -22,10 +22,11 @@ def max_pages(cfg):
 # (units, row blocks, replicas, CTAs, merge warps per row), worked out by hand:
 #   units = B * Hkv * ceil(T*G/128); replicas 4 for M <= 32, 2 for M <= 64;
 #   CTAs = min(152, units * ceil(max_pages*P/64));
-#   merge warps from (CTAs // units + 2) * replicas: > 12 -> 4, > 6 -> 2, else 1.
+#   merge warps from CTAs // units + 1 + replicas (prefix CTAs fold their row
+#   copies in their last segment): > 12 -> 4, > 6 -> 2, else 1.
 EXPECTED = {
-    "tiny": (2, 1, 4, 4, 4),          # M = 16; 2 units x 2 steps = 4 CTAs; (2+2)*4 = 16
-    "llama8b": (8, 1, 2, 152, 4),     # M = 48; (19+2)*2 = 42
+    "tiny": (2, 1, 4, 4, 2),          # M = 16; 2 units x 2 steps = 4 CTAs; 2 + 1 + 4 = 7
+    "llama8b": (8, 1, 2, 152, 4),     # M = 48; 19 + 1 + 2 = 22
 }
 
 def test_plan_llama8b_and_tiny_by_hand():
@@ -37,15 +38,15 @@ def test_plan_llama8b_and_tiny_by_hand():
 
 
 def test_plan_other_workloads_by_hand():
-    # llama70b: M = 8 * 8 = 64 -> 2 replicas; units 16*8 = 128; 152 // 128 = 1 -> (1+2)*2 = 6
+    # llama70b: M = 8 * 8 = 64 -> 2 replicas; units 16*8 = 128; 152 // 128 = 1 -> 1+1+2 = 4
     c = CONFIGS["llama70b"]
     p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
     assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (128, 2, 152, 1)
-    # chain: M = 4 * 4 = 16 -> 4 replicas; units 512; (0+2)*4 = 8 -> 2 warps
+    # chain: M = 4 * 4 = 16 -> 4 replicas; units 512; 0 + 1 + 4 = 5 -> 1 warp
     c = CONFIGS["chain"]
     p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
-    assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (512, 4, 152, 2)
-    # maverick: M = 16 * 5 = 80 -> 1 copy; units 32; (4+2)*1 = 6 -> 1 warp
+    assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (512, 4, 152, 1)
+    # maverick: M = 16 * 5 = 80 -> 1 copy; units 32; 4 + 1 + 1 = 6 -> 1 warp
     c = CONFIGS["maverick"]
     p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
     assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (32, 1, 152, 1)
