@@ -342,7 +342,11 @@ typedef struct tree_attn_plan_info {
     int n_ctas;              /* persistent prefix-pass CTAs                           */
     int merge_warps_per_row; /* warps that merge one query row (1, 2 or 4)            */
     long long max_steps;     /* 64-token work-line steps if every sequence were full */
+                             /* (+1 per unit when the tree rides on the prefix pass) */
     size_t workspace_bytes;  /* partial-result slots for this n_ctas                 */
+    int tree_in_prefix;      /* 1: the prefix pass attends the tree tokens too (one   */
+                             /* masked chunk per unit; small, latency-bound calls);   */
+                             /* 0: the suffix/merge kernel attends them               */
 } tree_attn_plan_info;
 
 TREE_ATTN_API int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size,

@@ -188,7 +188,21 @@ struct PrefixArgs {
     // is non-zero; seq_lens then counts every key in the cache, tree included.
     const uint8_t* dense;
     int dense_cols;
+    // Tree tokens on the work line (TreeMode; kTreeNone for DENSE kernels):
+    // their mask bits come from `mask` ([T] or [B][T] by mask_stride) or are
+    // built from `parents` (stride 0 or T), and are then also written to
+    // mask_out when it is not null.
+    int tmode;
+    const uint64_t* mask;
+    int mask_stride;
+    const int32_t* parents;
+    int parents_stride;
+    uint64_t* mask_out;
 };
+
+// Kernel variants of the prefix pass: the tree modes of layout.h, plus the
+// one-pass form under an explicit byte mask.
+constexpr int kModeDense = 3;
 
 __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
 #pragma unroll
@@ -208,7 +222,7 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
         int n = 0;
         if (b < a.B) {
             bool bad;
-            n = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+            n = unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
             if (bad && blockIdx.x == 0) report(a.status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
         }
         tot += __reduce_add_sync(kFull, n);
@@ -226,7 +240,7 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
             if (b < a.B) {
                 bool bad;
                 n = static_cast<long long>(upb) *
-                    chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+                    unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
             }
             const long long incl = warp_incl_scan(n, lane);
             const long long excl = incl - n;
@@ -273,11 +287,15 @@ __device__ __forceinline__ int blocks_of(const Segment& sg) {
     return (sg.chunk_end - sg.chunk_begin + 1) / 2;
 }
 
-template <int D, int F, bool DENSE>
+template <int D, int F, int MODE>
 __global__ void __launch_bounds__(192, 1)
     prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const PrefixArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_tk,
+                       const __grid_constant__ CUtensorMap tm_tv, const PrefixArgs a) {
     using S = PrefixShape<D>;
+    constexpr bool DENSE = MODE == kModeDense;
+    constexpr int TM = DENSE ? kTreeNone : MODE;  // tree mode of the work line
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -334,7 +352,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1);
+                   misc->x1, TM, a.T);
             const uint64_t pol = ptx::policy_evict_first();
             const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
             const int nsub = kChunk / Pb;                // boxes per 64-token step
@@ -344,7 +362,11 @@ __global__ void __launch_bounds__(192, 1)
             while (ok && w.next(sg)) {
                 bool bad;
                 const int L = clamp_seq_len(a.seq_lens[sg.b], a.P, a.max_pages, bad);
-                const int npages = (L + a.P - 1) / a.P;
+                // Pages holding this unit's keys: the prefix, and for
+                // kTreeInCache the tree tokens padded after it.
+                int npages = (L + a.P - 1) / a.P;
+                if (TM == kTreeInCache) npages = min(a.max_pages, (L + a.T + a.P - 1) / a.P);
+                const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
                 const int32_t* bt = a.block_table + static_cast<size_t>(sg.b) * a.max_pages;
                 for (int ch = sg.chunk_begin; ch < sg.chunk_end; ch += 2, ++jj) {
                     const int nh = min(2, sg.chunk_end - ch);  // 64-token steps in this block
@@ -362,7 +384,12 @@ __global__ void __launch_bounds__(192, 1)
                     int ys[8];
                     int rows[8];
                     int nl = 0;
+                    int tree_half = -1;  // half of the block holding the tree chunk
                     for (int hh = 0; hh < nh; ++hh) {
+                        if (TM == kTreeChunk && ch + hh == tree_ch) {
+                            tree_half = hh;
+                            continue;
+                        }
                         for (int i = 0; i < nsub; ++i) {
                             const int tok = (ch + hh) * kChunk + i * Pb;
                             const int lp = tok / a.P;
@@ -378,7 +405,9 @@ __global__ void __launch_bounds__(192, 1)
                         }
                     }
                     const uint32_t fb = bar(S::KV_FULL + s);
-                    const uint32_t bytes = static_cast<uint32_t>(nl * Pb * 128 * S::DH * 2);
+                    // a tree chunk is one 64-row box per 64 columns of K and of V
+                    const uint32_t bytes = static_cast<uint32_t>(
+                        (nl * Pb + (tree_half >= 0 ? kChunk : 0)) * 128 * S::DH * 2);
                     if (bytes != 0) {
                         ptx::mbar_arrive_expect_tx(fb, bytes);
                     } else {
@@ -393,6 +422,18 @@ __global__ void __launch_bounds__(192, 1)
                                              ys[l], fb, pol);
                             ptx::tma_load_2d(vst + h * S::HALF_BYTES + rows[l] * 128, &tm_v, h * 64,
                                              ys[l], fb, pol);
+                        }
+                    }
+                    if (TM == kTreeChunk && tree_half >= 0) {
+                        // Tree tokens 0..63 of (b, hk): rows b*T + j of the
+                        // [B*T][Hkv][d] buffers (rows past the tree are other
+                        // sequences' tokens or zero fill; they are masked and
+                        // their V rows zeroed).
+#pragma unroll
+                        for (int h = 0; h < S::DH; ++h) {
+                            const uint32_t off = h * S::HALF_BYTES + tree_half * kChunk * 128;
+                            ptx::tma_load_3d(kst + off, &tm_tk, h * 64, sg.hk, sg.b * a.T, fb, pol);
+                            ptx::tma_load_3d(vst + off, &tm_tv, h * 64, sg.hk, sg.b * a.T, fb, pol);
                         }
                     }
                 }
@@ -412,7 +453,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1);
+                   misc->x1, TM, a.T);
             const uint32_t idesc_qk = idesc_bf16_f32(kRows, kBlock, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
             uint32_t jj = 0, kk = 0;  // blocks of earlier segments, segments done
@@ -509,7 +550,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         Walker w;
         w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-               misc->x1);
+               misc->x1, TM, a.T);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
             const bool ok = ptx::mbar_wait(b, parity);
             const bool all = __all_sync(kFull, ok && !*abort_flag);
@@ -565,20 +606,99 @@ __global__ void __launch_bounds__(192, 1)
             const bool warp_any = (warp * 32) % R < Mrb;
             bool bad;
             const int L = clamp_seq_len(a.seq_lens[cur.b], a.P, a.max_pages, bad);
+            const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
+            // Ancestor bits of this row's tree node (tree modes): given, or
+            // built here from the parent array by this warp (pointer
+            // jumping, as in tree_mask_kernel).
+            uint64_t tbits = 0;
+            if constexpr (TM != kTreeNone) {
+                const int t = row_ok ? (cur.rb * kRows + lr) / a.G : 0;
+                if (a.parents != nullptr) {
+                    uint64_t anc[2];
+                    const bool bad_tree = warp_tree_mask(
+                        a.parents + static_cast<size_t>(cur.b) * a.parents_stride, a.T, lane, anc);
+                    tbits = pick64(anc[0], anc[1], t);
+                    // One warp per tree reports and writes the masks out: the
+                    // one holding the tree of the sequence's first unit.
+                    bool bad_l;
+                    const bool writer =
+                        warp == 0 && cur.unit == cur.b * upb &&
+                        cur.chunk_end ==
+                            unit_chunks(a.seq_lens[cur.b], a.P, a.max_pages, TM, a.T, bad_l) &&
+                        (a.parents_stride != 0 || cur.b == 0);
+                    if (writer && bad_tree && lane == 0)
+                        report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
+                    if (writer && a.mask_out != nullptr) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int i = lane + 32 * hh;
+                            if (i < a.T)
+                                a.mask_out[static_cast<size_t>(cur.b) * a.parents_stride + i] =
+                                    anc[hh];
+                        }
+                    }
+                } else if (row_ok) {
+                    tbits = a.mask[static_cast<size_t>(cur.b) * a.mask_stride + t];
+                }
+                if (a.T < 64) tbits &= (1ull << a.T) - 1ull;
+            }
+            // Keys of chunk c that this row may attend (bit i = key i): the
+            // committed prefix unmasked, the tree tokens by the ancestor bits,
+            // nothing past the data or outside this segment.
+            auto chunk_vis = [&](int c) -> uint64_t {
+                if (c >= cur.chunk_end) return 0ull;
+                if (TM == kTreeChunk && c == tree_ch) return tbits;
+                const long long rem = static_cast<long long>(L) - static_cast<long long>(c) * kChunk;
+                uint64_t v = rem >= kChunk ? ~0ull : (rem <= 0 ? 0ull : ((1ull << rem) - 1ull));
+                if (TM == kTreeInCache) {
+                    if (rem >= 0)
+                        v |= rem < 64 ? (tbits << rem) : 0ull;
+                    else
+                        v |= -rem < 64 ? (tbits >> -rem) : 0ull;
+                }
+                return v;
+            };
+            // Rows of chunk c that hold keys (the rest is stale or foreign data
+            // whose V rows are zeroed before P.V).
+            auto chunk_rows = [&](int c) -> int {
+                if (c >= cur.chunk_end) return 0;
+                if (TM == kTreeChunk && c == tree_ch) return a.T;
+                const long long e = static_cast<long long>(L) + (TM == kTreeInCache ? a.T : 0) -
+                                    static_cast<long long>(c) * kChunk;
+                return e >= kChunk ? kChunk : (e <= 0 ? 0 : static_cast<int>(e));
+            };
             float m_ref = kNegInf;  // base-2 reference; -inf until a key is seen
             float l_sum = 0.f;
-            // Explicit-mask form only: the sum of the probabilities as the
-            // P.V product sees them (bf16).  Such a row may hold just a few
-            // keys (tree tokens after an empty prefix), where the rounding
-            // of P does not average out; the epilogue rescales the row's
-            // accumulator by l_sum / l_rnd, so that out keeps a consistent
-            // numerator and denominator while lse keeps the exact sum.
-            float l_rnd = 0.f;
+            // The probabilities enter P.V as bf16.  In blocks holding tree
+            // keys (and everywhere under an explicit mask) a row may see just
+            // a few keys -- tree tokens after a short prefix -- where that
+            // rounding does not average out, so l_err sums bf16(p) - p there;
+            // the epilogue rescales the row's accumulator by
+            // l_sum / (l_sum + l_err): out keeps a consistent numerator and
+            // denominator, while lse keeps the exact sum.
+            float l_err = 0.f;
             for (int ch = cur.chunk_begin; ch < cur.chunk_end; ch += 2, ++jj) {
                 const bool first = ch == cur.chunk_begin;
                 const int nh = min(2, cur.chunk_end - ch);
-                const int n_valid = min(nh * kChunk, L - ch * kChunk);
-                const int nv = n_valid - k0;  // valid keys in this replica's range (may be <= 0)
+                // Two whole chunks of committed prefix: every key is there and
+                // visible to every row (the common case, decided per block).
+                const bool plain = nh == 2 && static_cast<long long>(ch + 2) * kChunk <= L;
+                // Otherwise: visibility of this thread's KF keys (k0 .. k0 + KF - 1).
+                uint64_t vis0 = ~0ull, vis1 = ~0ull;
+                int rows0 = kChunk, rows1 = kChunk;
+                if (!plain) {
+                    if constexpr (KF == 128) {
+                        vis0 = chunk_vis(ch);
+                        vis1 = chunk_vis(ch + 1);
+                    } else if constexpr (KF == 64) {
+                        vis0 = chunk_vis(ch + g) | 0ull;
+                    } else {
+                        vis0 = (chunk_vis(ch + (g >> 1)) >> ((g & 1) * 32)) | 0xffffffff00000000ull;
+                    }
+                    rows0 = chunk_rows(ch);
+                    rows1 = chunk_rows(ch + 1);
+                }
+                const bool all_vis = vis0 == ~0ull && (KF < 128 || vis1 == ~0ull);
                 // Explicit mask bytes of this row's keys, fetched before the
                 // scores are waited for (16 keys per vector).
                 uint4 mbits[DENSE ? KF / 16 : 1];
@@ -616,6 +736,15 @@ __global__ void __launch_bounds__(192, 1)
                 // (scale > 0, so the max of the raw scores gives the max of x).
                 float alpha = 1.f;
                 bool rescale = false;
+                if (!all_vis) {
+                    // Keys this row may not see score -inf: they add nothing
+                    // to the max or the sum, and their probabilities are 0.
+#pragma unroll
+                    for (int i = 0; i < KF; ++i) {
+                        const uint64_t bit = i < 64 ? (vis0 >> i) : (vis1 >> (i - 64));
+                        if ((bit & 1ull) == 0) s[i] = kNegInf;
+                    }
+                }
                 if constexpr (DENSE) {
                     // Hidden keys score -inf: they add nothing to the max or
                     // the sum, and their probabilities are exactly 0.
@@ -635,14 +764,8 @@ __global__ void __launch_bounds__(192, 1)
                     float mp[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) mp[u] = kNegInf;
-                    if (nv >= KF) {
 #pragma unroll
-                        for (int i = 0; i < KF; ++i) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < KF; ++i)
-                            if (i < nv) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
-                    }
+                    for (int i = 0; i < KF; ++i) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
                     float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
                     mx *= a.scale_log2;
@@ -654,36 +777,32 @@ __global__ void __launch_bounds__(192, 1)
                         alpha = ptx::ex2(m_ref - mx);
                         m_ref = mx;
                         l_sum *= alpha;
-                        l_rnd *= alpha;
+                        l_err *= alpha;
                         rescale = true;
                     }
                     const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;
                     float sp[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) sp[u] = 0.f;
-                    if constexpr (DENSE) {
-                        // Sum both the exact and the bf16-rounded values (see
-                        // the epilogue).
+                    const bool track = DENSE || (TM != kTreeNone && !plain &&
+                                                 ((TM == kTreeChunk && ch + nh > tree_ch) ||
+                                                  (TM == kTreeInCache && (ch + nh) * kChunk > L)));
+                    if (track) {
+                        // Sum the exact values and the rounding errors of the
+                        // bf16 values P.V will use (see the epilogue).
                         float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int i = 0; i < KF; ++i) {
-                            const float e =
-                                (i < nv) ? ptx::ex2(fmaf(s[i], a.scale_log2, neg_m)) : 0.f;
+                            const float e = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
                             s[i] = __bfloat162float(__float2bfloat16_rn(e));
                             sp[i & 7] += e;
-                            sr[i & 3] += s[i];
+                            sr[i & 3] += s[i] - e;
                         }
-                        l_rnd += (sr[0] + sr[1]) + (sr[2] + sr[3]);
-                    } else if (nv >= KF) {
-#pragma unroll
-                        for (int i = 0; i < KF; ++i) {
-                            s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
-                            sp[i & 7] += s[i];
-                        }
+                        l_err += (sr[0] + sr[1]) + (sr[2] + sr[3]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < KF; ++i) {
-                            s[i] = (i < nv) ? ptx::ex2(fmaf(s[i], a.scale_log2, neg_m)) : 0.f;
+                            s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
                             sp[i & 7] += s[i];
                         }
                     }
@@ -728,18 +847,20 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     ptx::tmem_wait_st();
                 }
-                if (n_valid < kBlock) {
-                    // Slots past the sequence end hold stale data; zero their
-                    // V rows so 0 * garbage cannot reach O.
+                if (rows0 < kChunk || rows1 < kChunk) {
+                    // Rows past the keys of each chunk hold stale or foreign
+                    // data; zero their V rows so 0 * garbage cannot reach O.
                     if (!wait_all(bar(S::KV_FULL + jj % S::NS), (jj / S::NS) & 1)) {
                         ok = false;
                         break;
                     }
                     const uint32_t vst =
                         sb + S::OFF_STAGE + (jj % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
-                    const int items = (kBlock - n_valid) * S::DH * 8;
+                    const int n0 = kChunk - rows0;
+                    const int items = (n0 + kChunk - rows1) * S::DH * 8;
                     for (int it = r; it < items; it += 128) {
-                        const int row = n_valid + it / (S::DH * 8);
+                        const int idx = it / (S::DH * 8);
+                        const int row = idx < n0 ? rows0 + idx : kChunk + rows1 + (idx - n0);
                         const int rem = it % (S::DH * 8);
                         st_shared_v4(vst + (rem >> 3) * S::HALF_BYTES + row * 128 + (rem & 7) * 16,
                                      0u, 0u, 0u, 0u);
@@ -763,7 +884,8 @@ __global__ void __launch_bounds__(192, 1)
             ptx::tc_fence_after();
             float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
             const uint32_t to = lane_base + S::TM_O;
-            const float acc_scale = (DENSE && l_rnd > 0.f) ? l_sum / l_rnd : 1.f;
+            const float acc_scale =
+                (l_err != 0.f && l_sum + l_err > 0.f) ? l_sum / (l_sum + l_err) : 1.f;
             if (F > 1 && !have_next) {
                 // Last segment of this CTA: every MMA and copy has completed,
                 // so the K/V ring is free.  Fold the F row copies into copy 0
@@ -916,6 +1038,9 @@ struct MergeArgs {
     const int32_t* parents;
     int parents_stride;
     uint64_t* mask_out;
+    // TreeMode of the prefix pass: with the tree on its work line there is
+    // no suffix pass here.
+    int tmode;
 };
 
 template <int E>
@@ -1006,15 +1131,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         const int32_t l1 = b1 < a.B ? a.seq_lens[b1] : 0;
         const int32_t l2 = b2 < a.B ? a.seq_lens[b2] : 0;
         bool bad;
-        const int n1 = b1 < a.B ? chunks_of(clamp_seq_len(l1, a.P, a.max_pages, bad)) : 0;
-        const int n2 = b2 < a.B ? chunks_of(clamp_seq_len(l2, a.P, a.max_pages, bad)) : 0;
+        const int n1 = b1 < a.B ? unit_chunks(l1, a.P, a.max_pages, a.tmode, a.T, bad) : 0;
+        const int n2 = b2 < a.B ? unit_chunks(l2, a.P, a.max_pages, a.tmode, a.T, bad) : 0;
         W += __reduce_add_sync(kFull, n1 + n2);
         base_b += __reduce_add_sync(kFull, (b1 < b ? n1 : 0) + (b2 < b ? n2 : 0));
     }
     W *= upb;
     base_b *= upb;
     bool bad;
-    const int nch = chunks_of(clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad));
+    const int nch = unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
     int c_first = 0, c_last = -1;
     // A prefix CTA folds its F row copies into one partial in its last
     // segment.  Every CTA before c_last ends inside this unit; c_last does
@@ -1037,7 +1162,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     // Tree mask of this row's node: given, or built here from the parent
     // array (one warp's pointer jumping, as in tree_mask_kernel).
     uint64_t bits = 0;
-    if (a.parents != nullptr && sub == 0) {
+    const bool suffix_here = a.tmode == kTreeNone;
+    if (suffix_here && a.parents != nullptr && sub == 0) {
         uint64_t anc[2];
         const bool bad_tree = warp_tree_mask(
             a.parents + static_cast<size_t>(b) * a.parents_stride, a.T, lane, anc);
@@ -1054,11 +1180,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
                 if (i < a.T) a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
             }
         }
-    } else if (a.mask != nullptr && active && sub == 0) {
+    } else if (suffix_here && a.mask != nullptr && active && sub == 0) {
         bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
     }
     if (a.T < 64) bits &= (1ull << a.T) - 1ull;
-    if (active && sub == 0 && (a.mask != nullptr || a.parents != nullptr)) {
+    if (suffix_here && active && sub == 0 && (a.mask != nullptr || a.parents != nullptr)) {
         float qv[E];
         load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
         int L_b = 0;
@@ -1287,16 +1413,19 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 
 template <int D>
 cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void* tmap_v,
-                            cudaStream_t stream) {
+                            const void* tmap_tk, const void* tmap_tv, cudaStream_t stream) {
     using S = PrefixShape<D>;
     static int configured_for = -1;  // device on which the smem opt-in was applied
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        for (auto k : {prefix_pass_kernel<D, 1, false>, prefix_pass_kernel<D, 2, false>,
-                       prefix_pass_kernel<D, 4, false>, prefix_pass_kernel<D, 1, true>,
-                       prefix_pass_kernel<D, 2, true>, prefix_pass_kernel<D, 4, true>}) {
+        for (auto k : {prefix_pass_kernel<D, 1, 0>, prefix_pass_kernel<D, 2, 0>,
+                       prefix_pass_kernel<D, 4, 0>, prefix_pass_kernel<D, 1, 1>,
+                       prefix_pass_kernel<D, 2, 1>, prefix_pass_kernel<D, 4, 1>,
+                       prefix_pass_kernel<D, 1, 2>, prefix_pass_kernel<D, 2, 2>,
+                       prefix_pass_kernel<D, 4, 2>, prefix_pass_kernel<D, 1, 3>,
+                       prefix_pass_kernel<D, 2, 3>, prefix_pass_kernel<D, 4, 3>}) {
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
             if (e != cudaSuccess) return e;
         }
@@ -1324,17 +1453,27 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.scale_log2 = v.scale_log2;
     pa.dense = v.dense;
     pa.dense_cols = v.dense_cols;
+    pa.tmode = v.dense != nullptr ? kTreeNone : v.tmode;
+    pa.mask = v.mask;
+    pa.mask_stride = v.mask_stride;
+    pa.parents = v.parents;
+    pa.parents_stride = v.parents_stride;
+    pa.mask_out = v.mask_out;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
+    const CUtensorMap& ttk = *static_cast<const CUtensorMap*>(tmap_tk);
+    const CUtensorMap& ttv = *static_cast<const CUtensorMap*>(tmap_tv);
     const int F = pa.RB == 1 ? replicas_of(M) : 1;
-    auto kernel = F == 4 ? prefix_pass_kernel<D, 4, false>
-                         : (F == 2 ? prefix_pass_kernel<D, 2, false>
-                                   : prefix_pass_kernel<D, 1, false>);
-    if (v.dense != nullptr)
-        kernel = F == 4 ? prefix_pass_kernel<D, 4, true>
-                        : (F == 2 ? prefix_pass_kernel<D, 2, true>
-                                  : prefix_pass_kernel<D, 1, true>);
-    return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, pa);
+    const int mode = v.dense != nullptr ? kModeDense : v.tmode;
+    using K = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefixArgs);
+    const K table[4][3] = {
+        {prefix_pass_kernel<D, 1, 0>, prefix_pass_kernel<D, 2, 0>, prefix_pass_kernel<D, 4, 0>},
+        {prefix_pass_kernel<D, 1, 1>, prefix_pass_kernel<D, 2, 1>, prefix_pass_kernel<D, 4, 1>},
+        {prefix_pass_kernel<D, 1, 2>, prefix_pass_kernel<D, 2, 2>, prefix_pass_kernel<D, 4, 2>},
+        {prefix_pass_kernel<D, 1, 3>, prefix_pass_kernel<D, 2, 3>, prefix_pass_kernel<D, 4, 3>}};
+    const K kernel = table[mode][F == 4 ? 2 : (F == 2 ? 1 : 0)];
+    return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, ttk, ttv,
+                      pa);
 }
 
 template <int D>
@@ -1372,7 +1511,9 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.parents = v.parents;
     ma.parents_stride = v.parents_stride;
     ma.mask_out = v.mask_out;
-    const Plan plan = make_plan(v.B, v.Hq, v.Hkv, v.T, v.P, v.max_pages, v.n_ctas, v.n_ctas);
+    ma.tmode = v.tmode;
+    const Plan plan =
+        make_plan(v.B, v.Hq, v.Hkv, v.T, v.P, v.max_pages, v.n_ctas, v.n_ctas, v.tmode);
     const long long units = plan.units;
     const int F = plan.F;
     ma.wpr = plan.merge_wpr;
@@ -1449,9 +1590,9 @@ cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64
 }
 
 cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
-                          cudaStream_t stream) {
-    if (a.d == 128) return launch_prefix_d<128>(a, tmap_k, tmap_v, stream);
-    return launch_prefix_d<64>(a, tmap_k, tmap_v, stream);
+                          const void* tmap_tk, const void* tmap_tv, cudaStream_t stream) {
+    if (a.d == 128) return launch_prefix_d<128>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+    return launch_prefix_d<64>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
 }
 
 cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream) {

@@ -37,6 +37,9 @@ struct VerifyArgs {
     const int32_t* parents;
     int parents_stride;
     uint64_t* mask_out;
+    // Where the prefix pass finds the tree tokens (TreeMode in layout.h):
+    // kTreeNone leaves them to the merge kernel (two-pass form).
+    int tmode;
 };
 
 // Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and
@@ -51,9 +54,11 @@ cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64
                               int32_t* status, cudaStream_t stream);
 
 // Enqueue the prefix pass (partials into a.ws).  `tmap_k`/`tmap_v` point at
-// encoded CUtensorMap objects (host memory, copied into the launch).
+// encoded CUtensorMap objects of the paged cache, `tmap_tk`/`tmap_tv` at
+// those of the tree K/V buffers (kTreeChunk; otherwise any valid maps).
+// All are host memory, copied into the launch.
 cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
-                          cudaStream_t stream);
+                          const void* tmap_tk, const void* tmap_tv, cudaStream_t stream);
 
 // Enqueue the suffix pass + merge (reads the partials in a.ws).
 cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream);

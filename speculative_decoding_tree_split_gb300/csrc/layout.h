@@ -90,6 +90,34 @@ TA_HD int clamp_seq_len(int32_t L, int P, int max_pages, bool& bad) {
 
 TA_HD int chunks_of(int L) { return (L + kChunk - 1) / kChunk; }
 
+// Where the draft-tree tokens sit on the work line:
+//   kTreeNone     not at all: the prefix pass alone (the merge kernel then
+//                 attends the tree tokens: the two-pass form);
+//   kTreeChunk    one extra 64-key chunk after the unit's prefix chunks,
+//                 loaded from the separate tree K/V buffers (token j in row j);
+//   kTreeInCache  the tree tokens follow the prefix in the paged cache
+//                 (positions L .. L+T-1), so the unit covers L + T positions.
+// In both tree modes the prefix keys stay unmasked and the tree keys are
+// masked per query row by the ancestor bits.
+enum TreeMode : int { kTreeNone = 0, kTreeChunk = 1, kTreeInCache = 2 };
+
+// Work-line steps of one unit of a sequence with L_raw committed tokens;
+// `bad` is set when the lengths had to be clamped to the block table.
+TA_HD int unit_chunks(int32_t L_raw, int P, int max_pages, int tmode, int T, bool& bad) {
+    const int L = clamp_seq_len(L_raw, P, max_pages, bad);
+    if (tmode == kTreeChunk) return chunks_of(L) + 1;
+    if (tmode == kTreeInCache) {
+        const long long cap = static_cast<long long>(max_pages) * P;
+        long long e = static_cast<long long>(L) + T;
+        if (e > cap) {
+            bad = true;
+            e = cap;
+        }
+        return chunks_of(static_cast<int>(e));
+    }
+    return chunks_of(L);
+}
+
 TA_HD long long cta_start(int c, long long W, int C) {
     return static_cast<long long>(c) * W / C;
 }
@@ -116,6 +144,7 @@ struct Segment {
 struct Walker {
     const int32_t* seq_lens;
     int B, P, max_pages, units_per_b, RB;
+    int tmode, T;    // TreeMode and tree size
     int b;           // current sequence
     long long base;  // work-line position of sequence b's first unit
     int nch;         // chunks per unit of sequence b
@@ -123,11 +152,14 @@ struct Walker {
 
     TA_HD int chunks_b(int bb) const {
         bool bad;
-        return chunks_of(clamp_seq_len(seq_lens[bb], P, max_pages, bad));
+        return unit_chunks(seq_lens[bb], P, max_pages, tmode, T, bad);
     }
 
     TA_HD void init(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
-                    long long base0, long long x0, long long x1_) {
+                    long long base0, long long x0, long long x1_, int tmode_ = kTreeNone,
+                    int T_ = 0) {
+        tmode = tmode_;
+        T = T_;
         seq_lens = sl;
         B = B_;
         P = P_;
@@ -169,11 +201,11 @@ struct Walker {
 // work-line base.  The kernels compute the same values with warp scans.
 inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, int upb, int C,
                         int c, long long& W, int& b0, long long& base0, long long& x0,
-                        long long& x1) {
+                        long long& x1, int tmode = kTreeNone, int T = 0) {
     long long tot = 0;
     for (int b = 0; b < B; ++b) {
         bool bad;
-        tot += chunks_of(clamp_seq_len(seq_lens[b], P, max_pages, bad));
+        tot += unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad);
     }
     W = tot * upb;
     x0 = cta_start(c, W, C);
@@ -184,7 +216,7 @@ inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, in
     for (int b = 0; b < B; ++b) {
         bool bad;
         const long long w = static_cast<long long>(upb) *
-                            chunks_of(clamp_seq_len(seq_lens[b], P, max_pages, bad));
+                            unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad);
         if (x0 < run + w) {
             b0 = b;
             base0 = run;
@@ -216,32 +248,50 @@ TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>
 //              would otherwise launch CTAs with nothing to do);
 //   F          query-row copies per tile when one 128-row block holds the
 //              unit's rows (small M: the softmax work per CTA is split);
+//   tmode      whether the tree tokens ride on the prefix pass (small,
+//              latency-bound calls) or are attended by the merge kernel;
 //   merge_wpr  warps per query row in the merge, from the partials a row
 //              expects: prefix CTAs per unit, +1 for a straddled end, +F
 //              for the unfolded copies of the last CTA.
 struct Plan {
     int G, M, RB, units, F, n_ctas, merge_wpr;
+    int tmode;  // TreeMode chosen for the call
     long long max_steps;
 };
 
+// Work-line steps per CTA at or below which the tree tokens ride on the
+// prefix pass (a call this small is latency-bound, and the merge's own tree
+// pass sits on its critical path); above it the merge kernel attends them.
+constexpr int kTreeInPrefixMaxSteps = 32;
+
+// tree_layout: kTreeNone for the prefix pass alone (two-pass API), else where
+// the call keeps the tree tokens (kTreeChunk: separate buffers; kTreeInCache:
+// padded into the cache); the plan picks that mode or kTreeNone.
 TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm_count,
-                     int n_ctas_req) {
+                     int n_ctas_req, int tree_layout = kTreeNone) {
     Plan p;
     p.G = Hq / Hkv;
     p.M = T * p.G;
     p.RB = (p.M + kRows - 1) / kRows;
     p.units = B * Hkv * p.RB;
     p.F = p.RB == 1 ? replicas_of(p.M) : 1;
-    p.max_steps = static_cast<long long>(p.units) *
-                  chunks_of(static_cast<int>(static_cast<long long>(max_pages) * P > (1LL << 30)
-                                                 ? (1LL << 30)
-                                                 : static_cast<long long>(max_pages) * P));
-    if (n_ctas_req > 0) {
-        p.n_ctas = n_ctas_req;
-    } else {
-        const long long cap = p.max_steps > 0 ? p.max_steps : 1;
-        p.n_ctas = sm_count < cap ? sm_count : static_cast<int>(cap);
-    }
+    const long long prefix_steps =
+        static_cast<long long>(p.units) *
+        chunks_of(static_cast<int>(static_cast<long long>(max_pages) * P > (1LL << 30)
+                                       ? (1LL << 30)
+                                       : static_cast<long long>(max_pages) * P));
+    auto ctas_for = [&](long long steps) -> int {
+        if (n_ctas_req > 0) return n_ctas_req;
+        const long long cap = steps > 0 ? steps : 1;
+        return sm_count < cap ? sm_count : static_cast<int>(cap);
+    };
+    p.tmode = kTreeNone;
+    if (tree_layout != kTreeNone &&
+        prefix_steps <= static_cast<long long>(kTreeInPrefixMaxSteps) *
+                            ctas_for(prefix_steps + p.units))
+        p.tmode = tree_layout;
+    p.max_steps = prefix_steps + (p.tmode == kTreeChunk ? p.units : 0);
+    p.n_ctas = ctas_for(p.max_steps);
     const long long units = p.units > 0 ? p.units : 1;
     // Prefix CTAs fold their F row copies in their last segment, so a row
     // sees about one partial per CTA plus the F copies of a straddling CTA.

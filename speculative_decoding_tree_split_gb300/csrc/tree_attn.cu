@@ -75,6 +75,23 @@ bool encode_pages(CUtensorMap* map, const void* base, long long rows, int d, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [B*T][Hkv][d] bf16 view of the tree K or V buffer, boxes of 64 tree
+// tokens x one head x 64 columns (the tree chunk of one unit).
+bool encode_tree(CUtensorMap* map, const void* base, int B, int T, int Hkv, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(B) * T};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(Hkv) * d * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Checks shared by the verify, prefix-pass and merge entry points.
 int check_common(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pages_per_seq,
                  float softmax_scale) {
@@ -85,11 +102,20 @@ int check_common(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pa
 }
 
 // CTAs of the prefix pass: the caller's count, else the kernel selector's.
+// The kernel selector's plan for a call (n_ctas > 0: the caller's count).
+// Returns false when the device cannot be queried.
+bool plan_call(int n_ctas, int B, int Hq, int Hkv, int T, int P, int max_pages, int tree_layout,
+               Plan& plan) {
+    const int sms = n_ctas > 0 ? n_ctas : sm_count();
+    if (sms <= 0) return false;
+    plan = make_plan(B, Hq, Hkv, T, P, max_pages, sms, n_ctas, tree_layout);
+    return true;
+}
+
+// CTAs of the prefix pass: the caller's count, else the kernel selector's.
 int resolve_ctas(int n_ctas, int B, int Hq, int Hkv, int T, int P, int max_pages) {
-    if (n_ctas > 0) return n_ctas;
-    const int sms = sm_count();
-    if (sms <= 0) return 0;
-    return make_plan(B, Hq, Hkv, T, P, max_pages, sms, 0).n_ctas;
+    Plan plan;
+    return plan_call(n_ctas, B, Hq, Hkv, T, P, max_pages, kTreeNone, plan) ? plan.n_ctas : 0;
 }
 
 float to_log2(float softmax_scale) {
@@ -100,11 +126,20 @@ int prefix_impl(VerifyArgs& a, const uint16_t* k_pages, const uint16_t* v_pages,
                 cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.num_pages) * a.Hkv * a.P;
     const int box_rows = a.P < kChunk ? a.P : kChunk;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, ttk, ttv;
     if (!encode_pages(&tk, k_pages, rows, a.d, box_rows) ||
         !encode_pages(&tv, v_pages, rows, a.d, box_rows))
         return TREE_ATTN_ERR_CUDA;
-    return launch_prefix(a, &tk, &tv, stream) == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+    if (a.tmode == kTreeChunk) {
+        if (!encode_tree(&ttk, a.tree_k, a.B, a.T, a.Hkv, a.d) ||
+            !encode_tree(&ttv, a.tree_v, a.B, a.T, a.Hkv, a.d))
+            return TREE_ATTN_ERR_CUDA;
+    } else {
+        ttk = tk;  // unused by the kernel in this mode
+        ttv = tv;
+    }
+    return launch_prefix(a, &tk, &tv, &ttk, &ttv, stream) == cudaSuccess ? TREE_ATTN_OK
+                                                                        : TREE_ATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -146,7 +181,8 @@ int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size, int max_
         return TREE_ATTN_ERR_SHAPE;
     const int sms = sm_count_hint > 0 ? sm_count_hint : sm_count();
     if (sms <= 0) return TREE_ATTN_ERR_CUDA;
-    const Plan p = make_plan(B, Hq, Hkv, T, page_size, max_pages_per_seq, sms, 0);
+    const Plan p = make_plan(B, Hq, Hkv, T, page_size, max_pages_per_seq, sms, 0, kTreeChunk);
+    out->tree_in_prefix = p.tmode != kTreeNone ? 1 : 0;
     out->units = p.units;
     out->row_blocks = p.RB;
     out->replicas = p.F;
@@ -287,13 +323,23 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
         !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || !aligned(lse, 4) || !aligned(mask, 8) || !aligned(status, 4))
         return TREE_ATTN_ERR_ALIGN;
-    n_ctas = resolve_ctas(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq);
-    if (n_ctas <= 0) return TREE_ATTN_ERR_CUDA;
+    // The tree tokens ride on the prefix pass's work line: one extra chunk
+    // per unit from the tree buffers, or the positions after the prefix when
+    // they are padded into the cache.  The explicit-mask form has no tree.
+    // The kernel selector decides which (small calls: on the line).
+    Plan plan;
+    if (!plan_call(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq,
+                   dense != nullptr ? kTreeNone : (tree_in_cache ? kTreeInCache : kTreeChunk),
+                   plan))
+        return TREE_ATTN_ERR_CUDA;
+    const int tmode = plan.tmode;
+    n_ctas = plan.n_ctas;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
         return TREE_ATTN_ERR_WORKSPACE;
 
     VerifyArgs a = {};
+    a.tmode = tmode;
     a.q = q;
     a.k_pages = k_pages;
     a.v_pages = v_pages;

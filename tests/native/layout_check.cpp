@@ -1,5 +1,7 @@
 // CPU check of the prefix-pass work partition in csrc/layout.h:
-//   * the segments of all CTAs cover every (unit, chunk) exactly once,
+//   * the segments of all CTAs cover every (unit, chunk) exactly once, with
+//     the tree tokens as one extra chunk per unit or as positions after the
+//     prefix (the tree modes),
 //   * partial-result slots (unit + cta) are unique and < units + CTAs,
 //   * the merge side's slot range for a unit (cta_of of the unit's first and
 //     last work-line positions) names exactly the CTAs that wrote it,
@@ -37,8 +39,8 @@ static unsigned next_rand() {
         }                                                    \
     } while (0)
 
-static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int F,
-                            const std::vector<int32_t>& sl) {
+static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int F, int tmode,
+                            int T, const std::vector<int32_t>& sl) {
     const int upb = Hkv * RB;
     std::set<std::tuple<int, int, int>> parts;  // (unit, CTA, copy) written
     std::map<std::pair<int, int>, int> covered;  // (unit, chunk) -> count
@@ -48,9 +50,9 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int 
     for (int c = 0; c < C; ++c) {
         int b0;
         long long base0, x0, x1;
-        plan_serial(sl.data(), B, P, maxp, upb, C, c, W, b0, base0, x0, x1);
+        plan_serial(sl.data(), B, P, maxp, upb, C, c, W, b0, base0, x0, x1, tmode, T);
         Walker w;
-        w.init(sl.data(), B, P, maxp, upb, RB, b0, base0, x0, x1);
+        w.init(sl.data(), B, P, maxp, upb, RB, b0, base0, x0, x1, tmode, T);
         Segment s;
         long long done = 0;
         std::vector<Segment> segs;
@@ -59,7 +61,7 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int 
             CHECK(s.chunk_end > s.chunk_begin, "empty segment");
             CHECK(s.unit == (s.b * Hkv + s.hk) * RB + s.rb, "unit index");
             bool bad;
-            const int nch = chunks_of(clamp_seq_len(sl[s.b], P, maxp, bad));
+            const int nch = unit_chunks(sl[s.b], P, maxp, tmode, T, bad);
             CHECK(s.chunk_end <= nch, "segment past the sequence");
             for (int ch = s.chunk_begin; ch < s.chunk_end; ++ch)
                 covered[std::make_pair(s.unit, ch)]++;
@@ -78,7 +80,7 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int 
     long long base = 0;
     for (int b = 0; b < B; ++b) {
         bool bad;
-        const int nch = chunks_of(clamp_seq_len(sl[b], P, maxp, bad));
+        const int nch = unit_chunks(sl[b], P, maxp, tmode, T, bad);
         for (int urel = 0; urel < upb; ++urel) {
             const int unit = b * upb + urel;
             for (int ch = 0; ch < nch; ++ch) {
@@ -161,13 +163,16 @@ int main() {
             else
                 sl[b] = next_rand() % (maxp * P + 1);
         }
-        for (int F = 1; F <= (RB == 1 ? 4 : 1); F *= 2) {
-            if (!check_partition(B, Hkv, RB, P, maxp, C, F, sl)) {
-                std::printf("  at trial %d (B=%d Hkv=%d RB=%d P=%d maxp=%d C=%d F=%d)\n", trial,
-                            B, Hkv, RB, P, maxp, C, F);
-                return 1;
+        const int T = 1 + next_rand() % 64;
+        for (int tmode = kTreeNone; tmode <= kTreeInCache; ++tmode)
+            for (int F = 1; F <= (RB == 1 ? 4 : 1); F *= 2) {
+                if (!check_partition(B, Hkv, RB, P, maxp, C, F, tmode, T, sl)) {
+                    std::printf(
+                        "  at trial %d (B=%d Hkv=%d RB=%d P=%d maxp=%d C=%d F=%d tmode=%d T=%d)\n",
+                        trial, B, Hkv, RB, P, maxp, C, F, tmode, T);
+                    return 1;
+                }
             }
-        }
     }
     std::printf("OK\n");
     return 0;

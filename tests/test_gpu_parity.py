@@ -181,7 +181,10 @@ def test_repeated_calls_are_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_two_pass_api_equals_verify():
+def test_two_pass_api_matches_oracle_and_verify(oracle):
+    # the two-pass form (prefix pass; suffix pass + merge) against the oracle
+    # and against tree_attn_verify, which attends the tree inside the prefix
+    # pass
     cfg = Config("t", B=2, Hq=16, Hkv=4, d=128, L=(0, 900), page=64, T=8, seed=35)
     wl = make_workload(cfg, seq_lens=[900, 77])
     x = to_dev(wl)
@@ -195,8 +198,10 @@ def test_two_pass_api_equals_verify():
     ta.suffix_merge(x["q"], x["seq_lens"], x["block_table"].shape[1], 64, x["tree_k"],
                     x["tree_v"], mask, ws, out, lse)
     torch.cuda.synchronize()
-    assert np.array_equal(out.float().cpu().numpy(), o1)
-    assert np.array_equal(lse.cpu().numpy(), l1)
+    o2, l2 = out.float().cpu().numpy(), lse.cpu().numpy()
+    ref_o, ref_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
+    assert np.abs(o2 - ref_o).max() <= OUT_TOL and np.abs(l2 - ref_l).max() <= LSE_TOL
+    assert np.abs(o2 - o1).max() <= OUT_TOL and np.abs(l2 - l1).max() <= LSE_TOL
 
 
 # ---------------------------------------------------------------------------
@@ -349,3 +354,14 @@ def test_many_partials_per_row(oracle, n_ctas):
     ref_o, ref_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
     assert np.abs(out - ref_o).max() <= OUT_TOL
     assert np.abs(lse - ref_l).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("n_ctas", [2, 100])
+def test_both_tree_placements(oracle, n_ctas):
+    # 8 units x 16 steps: with 2 CTAs (64 steps each) the merge kernel attends
+    # the tree; with 100 CTAs the prefix pass does (one masked chunk per unit)
+    cfg = Config("tp", B=2, Hq=16, Hkv=4, d=128, L=(0, 1000), page=64, T=12, seed=94)
+    wl = make_workload(cfg, seq_lens=[1000, 37])
+    p = ta.plan(2, 16, 4, 128, 12, 64, wl.max_pages_per_seq, n_ctas)
+    assert p["tree_in_prefix"] == (1 if n_ctas == 100 else 0)
+    compare_all(oracle, wl, n_ctas=n_ctas)

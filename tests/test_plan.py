@@ -21,13 +21,25 @@ def max_pages(cfg):
 
 # (units, row blocks, replicas, CTAs, merge warps per row), worked out by hand:
 #   units = B * Hkv * ceil(T*G/128); replicas 4 for M <= 32, 2 for M <= 64;
-#   CTAs = min(152, units * ceil(max_pages*P/64));
+#   CTAs = min(152, units * (ceil(max_pages*P/64) + 1)): the tree tokens are one
+#   more 64-key chunk of each unit's work;
 #   merge warps from CTAs // units + 1 + replicas (prefix CTAs fold their row
 #   copies in their last segment): > 12 -> 4, > 6 -> 2, else 1.
 EXPECTED = {
-    "tiny": (2, 1, 4, 4, 2),          # M = 16; 2 units x 2 steps = 4 CTAs; 2 + 1 + 4 = 7
+    "tiny": (2, 1, 4, 6, 2),          # M = 16; 2 units x 3 steps = 6 CTAs; 3 + 1 + 4 = 8
     "llama8b": (8, 1, 2, 152, 4),     # M = 48; 19 + 1 + 2 = 22
 }
+
+def test_plan_tree_placement_by_hand():
+    # llama8b: 8 units x 128 steps = 1024 <= 32 x 152 -> tree on the prefix pass;
+    # llama70b: 128 units x 128 = 16384 > 4864 -> the merge attends the tree
+    c = CONFIGS["llama8b"]
+    assert ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)["tree_in_prefix"] == 1
+    for name in ("llama70b", "chain", "maverick"):
+        c = CONFIGS[name]
+        p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+        assert p["tree_in_prefix"] == 0, name
+
 
 def test_plan_llama8b_and_tiny_by_hand():
     for name in ("tiny", "llama8b"):
@@ -61,7 +73,12 @@ def test_plan_invariants(B, Hq, Hkv, d, T, P, maxp):
     M = T * G
     assert p["row_blocks"] == (M + 127) // 128
     assert p["units"] == B * Hkv * p["row_blocks"]
-    assert p["max_steps"] == p["units"] * ((maxp * P + 63) // 64)
+    prefix_steps = p["units"] * ((maxp * P + 63) // 64)
+    # small calls (<= 32 steps per CTA) attend the tree in the prefix pass,
+    # one extra 64-key chunk per unit
+    want_tree = prefix_steps <= 32 * min(SMS, prefix_steps + p["units"])
+    assert p["tree_in_prefix"] == int(want_tree)
+    assert p["max_steps"] == prefix_steps + (p["units"] if want_tree else 0)
     assert 1 <= p["n_ctas"] <= min(SMS, max(1, p["max_steps"]))
     if p["row_blocks"] == 1:
         assert p["replicas"] * M <= 128 or p["replicas"] == 1
