@@ -198,6 +198,7 @@ struct PrefixArgs {
     const int32_t* parents;
     int parents_stride;
     uint64_t* mask_out;
+    int ovh;  // overhead slots per unit on the work line
 };
 
 // Kernel variants of the prefix pass: the tree modes of layout.h, plus the
@@ -222,7 +223,7 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
         int n = 0;
         if (b < a.B) {
             bool bad;
-            n = unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
+            n = unit_len(unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad), a.ovh);
             if (bad && blockIdx.x == 0) report(a.status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
         }
         tot += __reduce_add_sync(kFull, n);
@@ -240,7 +241,8 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
             if (b < a.B) {
                 bool bad;
                 n = static_cast<long long>(upb) *
-                    unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
+                    unit_len(unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad),
+                             a.ovh);
             }
             const long long incl = warp_incl_scan(n, lane);
             const long long excl = incl - n;
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1, TM, a.T);
+                   misc->x1, TM, a.T, a.ovh);
             const uint64_t pol = ptx::policy_evict_first();
             const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
             const int nsub = kChunk / Pb;                // boxes per 64-token step
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1, TM, a.T);
+                   misc->x1, TM, a.T, a.ovh);
             const uint32_t idesc_qk = idesc_bf16_f32(kRows, kBlock, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
             uint32_t jj = 0, kk = 0;  // blocks of earlier segments, segments done
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         Walker w;
         w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-               misc->x1, TM, a.T);
+               misc->x1, TM, a.T, a.ovh);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
             const bool ok = ptx::mbar_wait(b, parity);
             const bool all = __all_sync(kFull, ok && !*abort_flag);
@@ -1041,6 +1043,7 @@ struct MergeArgs {
     // TreeMode of the prefix pass: with the tree on its work line there is
     // no suffix pass here.
     int tmode;
+    int ovh;  // overhead slots per unit on the work line
 };
 
 template <int E>
@@ -1131,8 +1134,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         const int32_t l1 = b1 < a.B ? a.seq_lens[b1] : 0;
         const int32_t l2 = b2 < a.B ? a.seq_lens[b2] : 0;
         bool bad;
-        const int n1 = b1 < a.B ? unit_chunks(l1, a.P, a.max_pages, a.tmode, a.T, bad) : 0;
-        const int n2 = b2 < a.B ? unit_chunks(l2, a.P, a.max_pages, a.tmode, a.T, bad) : 0;
+        const int n1 =
+            b1 < a.B ? unit_len(unit_chunks(l1, a.P, a.max_pages, a.tmode, a.T, bad), a.ovh) : 0;
+        const int n2 =
+            b2 < a.B ? unit_len(unit_chunks(l2, a.P, a.max_pages, a.tmode, a.T, bad), a.ovh) : 0;
         W += __reduce_add_sync(kFull, n1 + n2);
         base_b += __reduce_add_sync(kFull, (b1 < b ? n1 : 0) + (b2 < b ? n2 : 0));
     }
@@ -1146,10 +1151,12 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     // only if its range stops at the unit's end.
     bool last_folded = F == 1;
     if (nch > 0) {
-        const long long ustart = base_b + static_cast<long long>(unit - b * upb) * nch;
+        // The unit's chunks, then its overhead slots (no chunks there).
+        const int len = unit_len(nch, a.ovh);
+        const long long ustart = base_b + static_cast<long long>(unit - b * upb) * len;
         c_first = cta_of(ustart, W, a.n_ctas);
         c_last = cta_of(ustart + nch - 1, W, a.n_ctas);
-        if (F > 1) last_folded = cta_start(c_last + 1, W, a.n_ctas) <= ustart + nch;
+        if (F > 1) last_folded = cta_start(c_last + 1, W, a.n_ctas) <= ustart + len;
     }
 
     // ---- suffix (sub-warp 0 of each row): softmax over the tree keys
@@ -1459,6 +1466,7 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.parents = v.parents;
     pa.parents_stride = v.parents_stride;
     pa.mask_out = v.mask_out;
+    pa.ovh = v.ovh;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
     const CUtensorMap& ttk = *static_cast<const CUtensorMap*>(tmap_tk);
@@ -1512,6 +1520,7 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     ma.parents_stride = v.parents_stride;
     ma.mask_out = v.mask_out;
     ma.tmode = v.tmode;
+    ma.ovh = v.ovh;
     const Plan plan =
         make_plan(v.B, v.Hq, v.Hkv, v.T, v.P, v.max_pages, v.n_ctas, v.n_ctas, v.tmode);
     const long long units = plan.units;

@@ -40,6 +40,7 @@ struct VerifyArgs {
     // Where the prefix pass finds the tree tokens (TreeMode in layout.h):
     // kTreeNone leaves them to the merge kernel (two-pass form).
     int tmode;
+    int ovh;  // overhead slots per unit on the work line (the kernel selector's)
 };
 
 // Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and

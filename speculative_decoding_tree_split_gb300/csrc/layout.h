@@ -134,6 +134,12 @@ TA_HD bool cta_has_work(int c, long long W, int C) {
     return cta_start(c, W, C) < cta_start(c + 1, W, C);
 }
 
+// Work-line length of a unit with nch chunks: the chunks, then `ovh` slots
+// that stand for the fixed cost of a segment (pipeline restart, epilogue,
+// partial store), so that a CTA whose range holds many short units gets
+// fewer chunks.  A unit with no chunks takes no room.
+TA_HD int unit_len(int nch, int ovh) { return nch > 0 ? nch + ovh : 0; }
+
 struct Segment {
     int b, hk, rb, unit;
     int chunk_begin, chunk_end;  // chunk indices within sequence b
@@ -145,9 +151,11 @@ struct Walker {
     const int32_t* seq_lens;
     int B, P, max_pages, units_per_b, RB;
     int tmode, T;    // TreeMode and tree size
+    int ovh;         // overhead slots per unit (see unit_len)
     int b;           // current sequence
     long long base;  // work-line position of sequence b's first unit
     int nch;         // chunks per unit of sequence b
+    int len;         // work-line length per unit of sequence b
     long long x, x1; // current position and end of this CTA's range
 
     TA_HD int chunks_b(int bb) const {
@@ -157,9 +165,10 @@ struct Walker {
 
     TA_HD void init(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
                     long long base0, long long x0, long long x1_, int tmode_ = kTreeNone,
-                    int T_ = 0) {
+                    int T_ = 0, int ovh_ = 0) {
         tmode = tmode_;
         T = T_;
+        ovh = ovh_;
         seq_lens = sl;
         B = B_;
         P = P_;
@@ -171,28 +180,37 @@ struct Walker {
         x = x0;
         x1 = x1_;
         nch = (x0 < x1_) ? chunks_b(b0) : 0;
+        len = unit_len(nch, ovh);
     }
 
     TA_HD bool next(Segment& s) {
-        if (x >= x1) return false;
-        while (x >= base + static_cast<long long>(units_per_b) * nch) {
-            base += static_cast<long long>(units_per_b) * nch;
-            ++b;
-            nch = chunks_b(b);
+        while (x < x1) {
+            while (x >= base + static_cast<long long>(units_per_b) * len) {
+                base += static_cast<long long>(units_per_b) * len;
+                ++b;
+                nch = chunks_b(b);
+                len = unit_len(nch, ovh);
+            }
+            const long long off = x - base;
+            const int urel = static_cast<int>(off / len);
+            const int pos = static_cast<int>(off % len);
+            const long long ubase = base + static_cast<long long>(urel) * len;
+            if (pos >= nch) {  // the unit's overhead slots: no chunks
+                x = ubase + len;
+                continue;
+            }
+            const long long cend = ubase + nch;
+            const long long e = x1 < cend ? x1 : cend;
+            s.b = b;
+            s.hk = urel / RB;
+            s.rb = urel % RB;
+            s.unit = b * units_per_b + urel;
+            s.chunk_begin = pos;
+            s.chunk_end = pos + static_cast<int>(e - x);
+            x = e;
+            return true;
         }
-        const long long off = x - base;
-        const int urel = static_cast<int>(off / nch);
-        const int ch = static_cast<int>(off % nch);
-        const long long uend = base + static_cast<long long>(urel + 1) * nch;
-        const long long e = x1 < uend ? x1 : uend;
-        s.b = b;
-        s.hk = urel / RB;
-        s.rb = urel % RB;
-        s.unit = b * units_per_b + urel;
-        s.chunk_begin = ch;
-        s.chunk_end = ch + static_cast<int>(e - x);
-        x = e;
-        return true;
+        return false;
     }
 };
 
@@ -201,11 +219,11 @@ struct Walker {
 // work-line base.  The kernels compute the same values with warp scans.
 inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, int upb, int C,
                         int c, long long& W, int& b0, long long& base0, long long& x0,
-                        long long& x1, int tmode = kTreeNone, int T = 0) {
+                        long long& x1, int tmode = kTreeNone, int T = 0, int ovh = 0) {
     long long tot = 0;
     for (int b = 0; b < B; ++b) {
         bool bad;
-        tot += unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad);
+        tot += unit_len(unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad), ovh);
     }
     W = tot * upb;
     x0 = cta_start(c, W, C);
@@ -216,7 +234,7 @@ inline void plan_serial(const int32_t* seq_lens, int B, int P, int max_pages, in
     for (int b = 0; b < B; ++b) {
         bool bad;
         const long long w = static_cast<long long>(upb) *
-                            unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad);
+                            unit_len(unit_chunks(seq_lens[b], P, max_pages, tmode, T, bad), ovh);
         if (x0 < run + w) {
             b0 = b;
             base0 = run;
@@ -256,8 +274,18 @@ TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>
 struct Plan {
     int G, M, RB, units, F, n_ctas, merge_wpr;
     int tmode;  // TreeMode chosen for the call
+    int ovh;    // overhead slots per unit on the work line (unit_len)
     long long max_steps;
 };
+
+// Overhead slots per unit: a segment switch costs about as much as 2 + F*M/24
+// 64-key steps (measured: the epilogue stores F*M rows of partials, then the
+// pipeline restarts).
+TA_HD int overhead_slots(int F, int M) {
+    const int rows = F * (M < kRows ? M : kRows);
+    const int o = 2 + rows / 24;
+    return o > 8 ? 8 : o;
+}
 
 // Work-line steps per CTA at or below which the tree tokens ride on the
 // prefix pass (a call this small is latency-bound, and the merge's own tree
@@ -290,6 +318,7 @@ TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm
         prefix_steps <= static_cast<long long>(kTreeInPrefixMaxSteps) *
                             ctas_for(prefix_steps + p.units))
         p.tmode = tree_layout;
+    p.ovh = overhead_slots(p.F, p.M);
     p.max_steps = prefix_steps + (p.tmode == kTreeChunk ? p.units : 0);
     p.n_ctas = ctas_for(p.max_steps);
     const long long units = p.units > 0 ? p.units : 1;

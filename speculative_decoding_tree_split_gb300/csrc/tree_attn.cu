@@ -101,7 +101,6 @@ int check_common(int B, int Hq, int Hkv, int d, int T, int page_size, int max_pa
     return TREE_ATTN_OK;
 }
 
-// CTAs of the prefix pass: the caller's count, else the kernel selector's.
 // The kernel selector's plan for a call (n_ctas > 0: the caller's count).
 // Returns false when the device cannot be queried.
 bool plan_call(int n_ctas, int B, int Hq, int Hkv, int T, int P, int max_pages, int tree_layout,
@@ -110,6 +109,13 @@ bool plan_call(int n_ctas, int B, int Hq, int Hkv, int T, int P, int max_pages, 
     if (sms <= 0) return false;
     plan = make_plan(B, Hq, Hkv, T, P, max_pages, sms, n_ctas, tree_layout);
     return true;
+}
+
+// Overhead slots per unit for these shapes (the kernel selector's choice).
+int ovh_for(int Hq, int Hkv, int T) {
+    const int M = T * (Hq / Hkv);
+    const int F = M <= kRows ? replicas_of(M) : 1;
+    return overhead_slots(F, M);
 }
 
 // CTAs of the prefix pass: the caller's count, else the kernel selector's.
@@ -235,6 +241,7 @@ int tree_attn_prefix_pass(const uint16_t* q, const uint16_t* k_pages, const uint
     a.max_pages = max_pages_per_seq;
     a.num_pages = num_pages;
     a.n_ctas = n_ctas;
+    a.ovh = ovh_for(Hq, Hkv, T);
     a.scale_log2 = to_log2(softmax_scale);
     return prefix_impl(a, k_pages, v_pages, static_cast<cudaStream_t>(stream));
 }
@@ -273,6 +280,7 @@ int tree_attn_suffix_merge(const uint16_t* q, const int32_t* seq_lens, int max_p
     a.P = page_size;
     a.max_pages = max_pages_per_seq;
     a.n_ctas = n_ctas;
+    a.ovh = ovh_for(Hq, Hkv, T);
     a.scale_log2 = to_log2(softmax_scale);
     return launch_merge(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TREE_ATTN_OK
                                                                            : TREE_ATTN_ERR_CUDA;
@@ -334,12 +342,14 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
         return TREE_ATTN_ERR_CUDA;
     const int tmode = plan.tmode;
     n_ctas = plan.n_ctas;
+    const int ovh = plan.ovh;
     if (workspace == nullptr || !aligned(workspace, 256) ||
         workspace_bytes < ws_bytes(B, Hq, Hkv, d, T, n_ctas))
         return TREE_ATTN_ERR_WORKSPACE;
 
     VerifyArgs a = {};
     a.tmode = tmode;
+    a.ovh = ovh;
     a.q = q;
     a.k_pages = k_pages;
     a.v_pages = v_pages;
