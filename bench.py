@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 # source whose SHA-256 is recorded with it (see profiles/).
 NCU_TRAFFIC = {
     # Llama-3.1-8B layer, mean of three launches of one ncu capture
-    "llama8b": ("7ed6147ffaa6b3b9", 33740800),
+    "llama8b": ("6940b45e4a49538c", 33747285),
 }
 
 
@@ -102,11 +102,13 @@ def measured_hbm_peak():
 
 
 def kernel_source_sha():
+    """SHA-256 prefix of the device sources the prefix-pass kernel is built from."""
     import hashlib
     h = hashlib.sha256()
-    with open(os.path.join(_ROOT, "speculative_decoding_tree_split_gb300", "csrc",
-                           "kernels.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("kernels.cu", "layout.h", "ptx.cuh"):
+        with open(os.path.join(_ROOT, "speculative_decoding_tree_split_gb300", "csrc", name),
+                  "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
