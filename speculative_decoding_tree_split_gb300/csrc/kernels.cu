@@ -1125,6 +1125,16 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         h = hk * a.G + rr % a.G;
     }
 
+    // Parent array of this row's tree (masks built here): lane l holds the
+    // parents of nodes l and l + 32.  Loaded now, used after the plan.
+    const bool suffix_here = a.tmode == kTreeNone;
+    int par0 = -1, par1 = -1;
+    if (suffix_here && a.parents != nullptr && sub == 0) {
+        const int32_t* pr = a.parents + static_cast<size_t>(b) * a.parents_stride;
+        if (lane < a.T) par0 = pr[lane];
+        if (lane + 32 < a.T) par1 = pr[lane + 32];
+    }
+
     // ---- work-line plan of this unit (inputs only): sequence lengths of
     // the whole batch, loaded 64 at a time.
     const int upb = a.Hkv * a.RB;
@@ -1167,18 +1177,29 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     // Tree mask of this row's node: given, or built here from the parent
-    // array (one warp's pointer jumping, as in tree_mask_kernel).
+    // array -- by walking the parent links up from node t (the row's warp
+    // holds the array in registers: one shuffle per ancestor).  A link that
+    // does not point to an earlier node ends the walk (that node is then a
+    // root, as in tree_mask_kernel, which reports it).
     uint64_t bits = 0;
-    const bool suffix_here = a.tmode == kTreeNone;
     if (suffix_here && a.parents != nullptr && sub == 0) {
-        uint64_t anc[2];
-        const bool bad_tree = warp_tree_mask(
-            a.parents + static_cast<size_t>(b) * a.parents_stride, a.T, lane, anc);
-        bits = pick64(anc[0], anc[1], t);
-        // One warp per tree reports and writes the masks out: the first
-        // unit's of the sequence (per-sequence trees) or of the batch.
+        for (int node = t, steps = 0; node >= 0 && steps < 64; ++steps) {
+            bits |= 1ull << node;
+            const int n0 = __shfl_sync(kFull, par0, node & 31);
+            const int n1 = __shfl_sync(kFull, par1, node & 31);
+            const int nxt = node < 32 ? n0 : n1;
+            node = (nxt >= -1 && nxt < node) ? nxt : -1;
+        }
+        // One warp per tree validates the array and writes the masks out:
+        // the first unit's of the sequence (per-sequence trees) or of the
+        // batch (pointer jumping over all nodes, as in tree_mask_kernel).
         const bool writer = unit == b * upb && blockIdx.y == 0 && warp == 0 &&
                             (a.parents_stride != 0 || b == 0);
+        uint64_t anc[2] = {0ull, 0ull};
+        bool bad_tree = false;
+        if (writer)
+            bad_tree = warp_tree_mask(a.parents + static_cast<size_t>(b) * a.parents_stride,
+                                      a.T, lane, anc);
         if (writer && bad_tree && lane == 0) report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
         if (writer && a.mask_out != nullptr) {
 #pragma unroll
