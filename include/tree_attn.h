@@ -235,6 +235,22 @@ TREE_ATTN_API int tree_attn_verify_paged_tree(const uint16_t *q, const uint16_t 
                                               int32_t *status, void *stream);
 
 /*
+ * tree_accept_commit -- tree_greedy_accept and tree_kv_commit in one launch
+ * (each commit CTA finds its sequence's path itself).  Arguments as the two
+ * calls; accept_len, accept_path and bonus_token are nullable here.  The
+ * result is the same as calling the two in turn.
+ */
+TREE_ATTN_API int tree_accept_commit(const uint64_t *mask, int mask_stride,
+                                     const int32_t *draft_tokens, const int32_t *target_tokens,
+                                     uint16_t *k_pages, uint16_t *v_pages,
+                                     const int32_t *block_table, int max_pages_per_seq,
+                                     const int32_t *seq_lens, const uint16_t *tree_k,
+                                     const uint16_t *tree_v, int32_t *accept_len,
+                                     int32_t *accept_path, int32_t *bonus_token,
+                                     int32_t *seq_lens_out, int B, int Hkv, int d, int T,
+                                     int page_size, int num_pages, int32_t *status, void *stream);
+
+/*
  * tree_dense_mask_build / tree_attn_verify_dense -- the one-pass form of tree
  * attention under an explicit mask: the "giant explicit mask" that split tree
  * attention replaces (pith.science review of arXiv 2508.08192, "What carries

@@ -35,6 +35,7 @@ from ._lib import (  # noqa: F401
     dense_mask_build,
     verify_dense,
     kv_commit,
+    accept_commit,
     version,
     workspace_size,
 )

@@ -53,6 +53,7 @@ EXPORTED = (
     "tree_attn_verify_dense",
     "tree_attn_plan",
     "tree_attn_verify_tree",
+    "tree_accept_commit",
 )
 
 
@@ -129,6 +130,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_verify_tree.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp,
                                           i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     lib.tree_attn_verify_tree.restype = i32
+    lib.tree_accept_commit.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp,
+                                       vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.tree_accept_commit.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
     if path == LIB_PATH:
@@ -493,6 +497,41 @@ def kv_commit(k_pages, v_pages, block_table, seq_lens, accept_path, accept_len, 
     if rc != 0:
         raise TreeAttnError("tree_kv_commit", rc)
     return seq_lens_out
+
+
+def accept_commit(mask, draft_tokens, target_tokens, k_pages, v_pages, block_table, seq_lens, *,
+                  tree_k=None, tree_v=None, accept_len=None, accept_path=None, bonus_token=None,
+                  seq_lens_out=None, status=None, stream=None):
+    """greedy_accept + kv_commit in one launch.  Returns (accept_len, accept_path,
+    bonus_token, seq_lens_out)."""
+    _check(mask, "mask", _BITS64)
+    _check(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    _check(target_tokens, "target_tokens", (torch.int32,), 2)
+    bf = (torch.bfloat16,)
+    _check(k_pages, "k_pages", bf, 4)
+    _check(v_pages, "v_pages", bf, 4)
+    _check(block_table, "block_table", (torch.int32,), 2)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1)
+    B, T = draft_tokens.shape
+    num_pages, Hkv, P, d = k_pages.shape
+    dev = draft_tokens.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if accept_path is None:
+        accept_path = torch.empty((B, T), dtype=torch.int32, device=dev)
+    if bonus_token is None:
+        bonus_token = torch.empty(B, dtype=torch.int32, device=dev)
+    if seq_lens_out is None:
+        seq_lens_out = torch.empty(B, dtype=torch.int32, device=dev)
+    stride = T if mask.dim() == 2 else 0
+    rc = load().tree_accept_commit(
+        _ptr(mask), stride, _ptr(draft_tokens), _ptr(target_tokens), _ptr(k_pages), _ptr(v_pages),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(tree_k), _ptr(tree_v),
+        _ptr(accept_len), _ptr(accept_path), _ptr(bonus_token), _ptr(seq_lens_out), B, Hkv, d, T,
+        P, num_pages, _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise TreeAttnError("tree_accept_commit", rc)
+    return accept_len, accept_path, bonus_token, seq_lens_out
 
 
 def prefix_pass(q, k_pages, v_pages, block_table, seq_lens, workspace, *, T=None,

@@ -46,21 +46,17 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
 // path is the deepest accepted node's mask; a tie on depth goes to the lower
 // index (the reduction key puts 255 - i under the depth).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(32 * kAcceptWarps)
-    greedy_accept_kernel(const uint64_t* __restrict__ mask, int mask_stride,
-                         const int32_t* __restrict__ draft, const int32_t* __restrict__ target,
-                         int B, int T, int32_t* __restrict__ accept_len,
-                         int32_t* __restrict__ accept_path, int32_t* __restrict__ bonus) {
-    ptx::grid_dep_launch();
-    ptx::grid_dep_wait();
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
-    if (b >= B) return;
-    const uint64_t live = T >= 64 ? ~0ull : (1ull << T) - 1ull;
-    const uint64_t* m = mask + static_cast<size_t>(b) * mask_stride;
-    const int32_t* dr = draft + static_cast<size_t>(b) * T;
-    const int32_t* tg = target + static_cast<size_t>(b) * T;
+struct Accepted {
+    int best;     // last node of the committed path, -1 if none
+    int n;        // nodes on the path
+    uint64_t mb;  // the path's nodes (the mask of `best`)
+};
 
+// One warp: the committed path of one sequence (m, dr, tg: its mask row,
+// draft and target tokens).
+__device__ __forceinline__ Accepted warp_greedy_accept(const uint64_t* m, const int32_t* dr,
+                                                       const int32_t* tg, int T, int lane) {
+    const uint64_t live = T >= 64 ? ~0ull : (1ull << T) - 1ull;
     uint64_t mi[2];
     bool ok[2];
 #pragma unroll
@@ -91,24 +87,45 @@ __global__ void __launch_bounds__(32 * kAcceptWarps)
         }
     }
     key = __reduce_max_sync(kFull, key);
-    const int best = key != 0 ? 255 - static_cast<int>(key & 255u) : -1;
-    const int src_lane = best >= 0 ? (best & 31) : 0;
+    Accepted r;
+    r.best = key != 0 ? 255 - static_cast<int>(key & 255u) : -1;
+    const int src_lane = r.best >= 0 ? (r.best & 31) : 0;
     const uint64_t lo = __shfl_sync(kFull, mi[0], src_lane);
     const uint64_t hi = __shfl_sync(kFull, mi[1], src_lane);
-    const uint64_t mb = best < 0 ? 0ull : (best < 32 ? lo : hi);
-    const int n = __popcll(mb);
-    int32_t* path = accept_path + static_cast<size_t>(b) * T;
+    r.mb = r.best < 0 ? 0ull : (r.best < 32 ? lo : hi);
+    r.n = __popcll(r.mb);
+    return r;
+}
+
+// The path's nodes root first, then -1 (one warp).
+__device__ __forceinline__ void write_path(int32_t* path, const Accepted& acc, int T, int lane) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int i = lane + 32 * h;
         if (i < T) {
-            if ((mb >> i) & 1ull) path[__popcll(mb & ((1ull << i) - 1ull))] = i;
-            if (i >= n) path[i] = -1;
+            if ((acc.mb >> i) & 1ull) path[__popcll(acc.mb & ((1ull << i) - 1ull))] = i;
+            if (i >= acc.n) path[i] = -1;
         }
     }
+}
+
+__global__ void __launch_bounds__(32 * kAcceptWarps)
+    greedy_accept_kernel(const uint64_t* __restrict__ mask, int mask_stride,
+                         const int32_t* __restrict__ draft, const int32_t* __restrict__ target,
+                         int B, int T, int32_t* __restrict__ accept_len,
+                         int32_t* __restrict__ accept_path, int32_t* __restrict__ bonus) {
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
+    if (b >= B) return;
+    const int32_t* tg = target + static_cast<size_t>(b) * T;
+    const Accepted acc = warp_greedy_accept(mask + static_cast<size_t>(b) * mask_stride,
+                                            draft + static_cast<size_t>(b) * T, tg, T, lane);
+    write_path(accept_path + static_cast<size_t>(b) * T, acc, T, lane);
     if (lane == 0) {
-        accept_len[b] = n;
-        bonus[b] = best >= 0 ? tg[best] : -1;
+        accept_len[b] = acc.n;
+        bonus[b] = acc.best >= 0 ? tg[acc.best] : -1;
     }
 }
 
@@ -150,13 +167,10 @@ __device__ __forceinline__ long long cache_offset(const CommitArgs& a, int b, in
     return ((static_cast<long long>(page) * a.Hkv + hk) * a.P + pos % a.P) * a.d + c * 8;
 }
 
-__global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(CommitArgs a) {
-    ptx::grid_dep_launch();
-    ptx::grid_dep_wait();
-    const int b = blockIdx.x;
-    const int hk = blockIdx.y;
+// CTA (b, hk) of the commit: path node k (path[k], k < n) to position L_b + k.
+__device__ __forceinline__ void commit_rows(const CommitArgs& a, int b, int hk, int n,
+                                            const int32_t* path) {
     const int tid = threadIdx.x;
-    int n = a.accept_len[b];
     if (n < 0 || n > a.T) {
         if (tid == 0 && hk == 0) report(a.status, TREE_ATTN_STATUS_BAD_PATH);
         n = 0;
@@ -170,7 +184,6 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(CommitArgs a)
     }
     const int vpr = a.d / 8;
     const int nvec = n * vpr;
-    const int32_t* path = a.accept_path + static_cast<size_t>(b) * a.T;
 
     uint4 kr[kCommitVecs], vr[kCommitVecs];
     bool have[kCommitVecs];
@@ -214,6 +227,52 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(CommitArgs a)
     }
     if (hk == 0 && tid == 0 && a.seq_lens_out != nullptr)
         a.seq_lens_out[b] = bad_len ? L_in : L + n;
+}
+
+__global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(CommitArgs a) {
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    const int b = blockIdx.x;
+    commit_rows(a, b, blockIdx.y, a.accept_len[b], a.accept_path + static_cast<size_t>(b) * a.T);
+}
+
+// Acceptance and commit in one launch: warp 0 of every CTA (b, hk) finds
+// sequence b's path (a few hundred cycles, so each CTA repeats it rather
+// than waiting for another kernel); CTA (b, 0) writes the acceptance out.
+struct AcceptArgs {
+    const uint64_t* mask;
+    int mask_stride;
+    const int32_t* draft;
+    const int32_t* target;
+    int32_t* accept_len;   // nullable
+    int32_t* accept_path;  // nullable
+    int32_t* bonus;        // nullable
+};
+
+__global__ void __launch_bounds__(kCommitThreads)
+    accept_commit_kernel(CommitArgs a, AcceptArgs g) {
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    __shared__ int32_t path[TREE_ATTN_MAX_T];
+    __shared__ int n_s;
+    const int b = blockIdx.x, hk = blockIdx.y;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int32_t* tg = g.target + static_cast<size_t>(b) * a.T;
+        const Accepted acc =
+            warp_greedy_accept(g.mask + static_cast<size_t>(b) * g.mask_stride,
+                               g.draft + static_cast<size_t>(b) * a.T, tg, a.T, lane);
+        write_path(path, acc, a.T, lane);
+        if (lane == 0) n_s = acc.n;
+        if (hk == 0) {
+            if (g.accept_path != nullptr)
+                write_path(g.accept_path + static_cast<size_t>(b) * a.T, acc, a.T, lane);
+            if (lane == 0 && g.accept_len != nullptr) g.accept_len[b] = acc.n;
+            if (lane == 0 && g.bonus != nullptr) g.bonus[b] = acc.best >= 0 ? tg[acc.best] : -1;
+        }
+    }
+    __syncthreads();
+    commit_rows(a, b, hk, n_s, path);
 }
 
 template <typename Kernel, typename... Args>
@@ -299,6 +358,59 @@ int tree_kv_commit(uint16_t* k_pages, uint16_t* v_pages, const int32_t* block_ta
     a.num_pages = num_pages;
     const cudaError_t e = launch_pdl(kv_commit_kernel, dim3(B, Hkv), dim3(kCommitThreads),
                                      static_cast<cudaStream_t>(stream), a);
+    return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
+}
+
+int tree_accept_commit(const uint64_t* mask, int mask_stride, const int32_t* draft_tokens,
+                       const int32_t* target_tokens, uint16_t* k_pages, uint16_t* v_pages,
+                       const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                       const uint16_t* tree_k, const uint16_t* tree_v, int32_t* accept_len,
+                       int32_t* accept_path, int32_t* bonus_token, int32_t* seq_lens_out, int B,
+                       int Hkv, int d, int T, int page_size, int num_pages, int32_t* status,
+                       void* stream) {
+    if (B < 0 || Hkv < 1 || Hkv > 65535 || (d != 64 && d != 128) || T < 1 ||
+        T > TREE_ATTN_MAX_T || max_pages_per_seq < 1 || num_pages < 1 ||
+        (mask_stride != 0 && mask_stride != T) ||
+        (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128))
+        return TREE_ATTN_ERR_SHAPE;
+    if (seq_lens_out != nullptr && seq_lens_out == seq_lens) return TREE_ATTN_ERR_SHAPE;
+    if (B == 0) return TREE_ATTN_OK;
+    if (!mask || !draft_tokens || !target_tokens || !k_pages || !v_pages || !block_table ||
+        !seq_lens || ((tree_k == nullptr) != (tree_v == nullptr)))
+        return TREE_ATTN_ERR_NULL;
+    if (!aligned(mask, 8) || !aligned(draft_tokens, 4) || !aligned(target_tokens, 4) ||
+        !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(tree_k, 16) ||
+        !aligned(tree_v, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+        !aligned(accept_len, 4) || !aligned(accept_path, 4) || !aligned(bonus_token, 4) ||
+        !aligned(seq_lens_out, 4) || !aligned(status, 4))
+        return TREE_ATTN_ERR_ALIGN;
+    CommitArgs a;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.tree_k = tree_k;
+    a.tree_v = tree_v;
+    a.accept_path = nullptr;
+    a.accept_len = nullptr;
+    a.seq_lens_out = seq_lens_out;
+    a.status = status;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.T = T;
+    a.P = page_size;
+    a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    AcceptArgs g;
+    g.mask = mask;
+    g.mask_stride = mask_stride;
+    g.draft = draft_tokens;
+    g.target = target_tokens;
+    g.accept_len = accept_len;
+    g.accept_path = accept_path;
+    g.bonus = bonus_token;
+    const cudaError_t e = launch_pdl(accept_commit_kernel, dim3(B, Hkv), dim3(kCommitThreads),
+                                     static_cast<cudaStream_t>(stream), a, g);
     return e == cudaSuccess ? TREE_ATTN_OK : TREE_ATTN_ERR_CUDA;
 }
 

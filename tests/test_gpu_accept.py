@@ -186,3 +186,30 @@ def test_bad_path_and_overflow_set_status():
     ta.kv_commit(k, v, bt, sl_far, path3, n3, tree_k=tk, tree_v=tv, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) in (ta.STATUS_BAD_SEQ_LEN, ta.STATUS_BAD_PAGE)
+
+
+@pytest.mark.parametrize("in_cache", [False, True], ids=["tree_buffers", "tree_in_cache"])
+@pytest.mark.parametrize("cfg,lens", COMMIT, ids=[c.name for c, _ in COMMIT])
+def test_fused_accept_commit_equals_two_calls(cfg, lens, in_cache):
+    wl, draft, target = _commit_inputs(cfg, lens, in_cache, 300 + cfg.seed)
+    masks = ta.mask_build_batched(wl.parents.cuda())
+    tk = None if in_cache else wl.tree_k.cuda()
+    tv = None if in_cache else wl.tree_v.cuda()
+    bt, sl = wl.block_table.cuda(), wl.seq_lens.cuda()
+    d, t = draft.cuda(), target.cuda()
+    k1, v1 = wl.k_pages.cuda(), wl.v_pages.cuda()
+    n1, p1, b1 = ta.greedy_accept(masks, d, t)
+    s1 = ta.kv_commit(k1, v1, bt, sl, p1, n1, tree_k=tk, tree_v=tv)
+    k2, v2 = wl.k_pages.cuda(), wl.v_pages.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n2, p2, b2, s2 = ta.accept_commit(masks, d, t, k2, v2, bt, sl, tree_k=tk, tree_v=tv,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for x, y in ((n1, n2), (p1, p2), (b1, b2), (s1, s2), (k1, k2), (v1, v2)):
+        assert torch.equal(x, y)
+    # and against the oracle directly
+    wn, wpath, wbonus = acc.greedy_accept_batch(wl.parents.numpy(), draft.numpy(),
+                                                target.numpy())
+    assert np.array_equal(n2.cpu().numpy(), wn) and np.array_equal(p2.cpu().numpy(), wpath)
+    assert np.array_equal(b2.cpu().numpy(), wbonus)
