@@ -365,3 +365,40 @@ def test_both_tree_placements(oracle, n_ctas):
     p = ta.plan(2, 16, 4, 128, 12, 64, wl.max_pages_per_seq, n_ctas)
     assert p["tree_in_prefix"] == (1 if n_ctas == 100 else 0)
     compare_all(oracle, wl, n_ctas=n_ctas)
+
+
+@pytest.mark.parametrize("per_seq", [False, True], ids=["shared", "per_seq"])
+def test_verify_tree_two_pass_form(oracle, per_seq):
+    # 16 x 8 units x 64 steps is more than 32 steps per CTA on any GB300, so
+    # the merge kernel attends the tree (masks built there from the parents)
+    cfg = Config("vt2", B=16, Hq=32, Hkv=8, d=128, L=4096, page=64, T=8, max_depth=3,
+                 max_branch=3, seed=95)
+    wl = make_workload(cfg, per_sequence_trees=per_seq)
+    p = ta.plan(16, 32, 8, 128, 8, 64, wl.max_pages_per_seq)
+    assert p["tree_in_prefix"] == 0
+    x = to_dev(wl)
+    mask = ta.mask_build_batched(x["parents"]) if per_seq else ta.mask_build(x["parents"])
+    verify = ta.verify_batched if per_seq else ta.verify
+    o1, l1 = verify(x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["seq_lens"],
+                    x["tree_k"], x["tree_v"], mask, softmax_scale=wl.scale)
+    mask_out = torch.zeros_like(mask)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o2, l2 = ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                            x["seq_lens"], x["tree_k"], x["tree_v"], x["parents"],
+                            mask_out=mask_out, status=status, softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(mask_out, mask)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    rows = sample_rows(cfg, 128, 95)
+    for b in sorted(set(rows[:, 0].tolist())):
+        sel = rows[rows[:, 0] == b]
+        s = wl.sequence(b)
+        m = oracle.tree_mask(s.parents.tolist())
+        loc = sel.copy()
+        loc[:, 0] = 0
+        ref_o, ref_l = oracle.verify_rows(s, m, loc)
+        got_o = o2.float().cpu().numpy()[sel[:, 0], sel[:, 1], sel[:, 2]]
+        got_l = l2.cpu().numpy()[sel[:, 0], sel[:, 1], sel[:, 2]]
+        assert np.abs(got_o - ref_o).max() <= OUT_TOL
+        assert np.abs(got_l - ref_l).max() <= LSE_TOL
