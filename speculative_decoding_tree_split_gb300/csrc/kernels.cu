@@ -166,6 +166,8 @@ struct PrefixShape {
     static_assert(TM_P + 2 * (kBlock / 2) <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
+    static_assert(kRows * (D + 4 + 2) * 4 <= NS * STAGE_BYTES,
+                  "the last segment's epilogue stages every row copy in the K/V ring");
 };
 
 struct PrefixMisc {
@@ -214,19 +216,36 @@ __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
     return v;
 }
 
+// Sequences whose work-line lengths the plan keeps in registers (32 per
+// entry): their seq_lens are read in one round trip, all loads in flight.
+constexpr int kPlanRegs = 4;
+
 // Total work W and this CTA's starting sequence / base (warp 0, all lanes).
 __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     const int upb = a.Hkv * a.RB;
+    auto len_of = [&](int32_t L_raw, bool report_bad) -> int {
+        bool bad;
+        const int n = unit_len(unit_chunks(L_raw, a.P, a.max_pages, a.tmode, a.T, bad), a.ovh);
+        if (report_bad && bad && blockIdx.x == 0) report(a.status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
+        return n;
+    };
+    // All loads first, so that they are in flight together.
+    int32_t lraw[kPlanRegs];
+#pragma unroll
+    for (int i = 0; i < kPlanRegs; ++i) {
+        const int b = 32 * i + lane;
+        lraw[i] = b < a.B ? a.seq_lens[b] : 0;
+    }
+    int nreg[kPlanRegs];
+#pragma unroll
+    for (int i = 0; i < kPlanRegs; ++i) nreg[i] = 32 * i + lane < a.B ? len_of(lraw[i], true) : 0;
     long long tot = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
+#pragma unroll
+    for (int i = 0; i < kPlanRegs; ++i)
+        if (32 * i < a.B) tot += __reduce_add_sync(kFull, nreg[i]);
+    for (int b0 = 32 * kPlanRegs; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
-        int n = 0;
-        if (b < a.B) {
-            bool bad;
-            n = unit_len(unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad), a.ovh);
-            if (bad && blockIdx.x == 0) report(a.status, TREE_ATTN_STATUS_BAD_SEQ_LEN);
-        }
-        tot += __reduce_add_sync(kFull, n);
+        tot += __reduce_add_sync(kFull, b < a.B ? len_of(a.seq_lens[b], true) : 0);
     }
     const long long W = tot * upb;
     const long long x0 = cta_start(blockIdx.x, W, a.n_ctas);
@@ -237,13 +256,12 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
         long long run = 0;
         for (int b0 = 0; b0 < a.B; b0 += 32) {
             const int b = b0 + lane;
-            long long n = 0;
-            if (b < a.B) {
-                bool bad;
-                n = static_cast<long long>(upb) *
-                    unit_len(unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad),
-                             a.ovh);
-            }
+            int nb = 0;
+#pragma unroll
+            for (int i = 0; i < kPlanRegs; ++i)
+                if (b0 == 32 * i) nb = nreg[i];
+            if (b0 >= 32 * kPlanRegs && b < a.B) nb = len_of(a.seq_lens[b], false);
+            const long long n = static_cast<long long>(upb) * nb;
             const long long incl = warp_incl_scan(n, lane);
             const long long excl = incl - n;
             const bool hit = (b < a.B) && (run + excl <= x0) && (x0 < run + incl);
@@ -358,12 +376,13 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t pol = ptx::policy_evict_first();
             const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
             const int nsub = kChunk / Pb;                // boxes per 64-token step
+            const int pshift = __ffs(a.P) - 1;           // page_size is a power of two
             uint32_t jj = 0;
             bool ok = true;
             Segment sg;
             while (ok && w.next(sg)) {
                 bool bad;
-                const int L = clamp_seq_len(a.seq_lens[sg.b], a.P, a.max_pages, bad);
+                const int L = clamp_seq_len(sg.len_raw, a.P, a.max_pages, bad);
                 // Pages holding this unit's keys: the prefix, and for
                 // kTreeInCache the tree tokens padded after it.
                 int npages = (L + a.P - 1) / a.P;
@@ -383,25 +402,41 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
+                    // Pages of this block (at most 2 steps x 4 boxes): every
+                    // block-table load is issued before any is used, so a block
+                    // costs one round trip to the table, not one per page.
+                    int pids[8];
+                    bool use[8];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int k = hh * 4 + i;
+                            const int tok = (ch + hh) * kChunk + i * Pb;
+                            const int lp = tok >> pshift;
+                            use[k] = hh < nh && i < nsub && lp < npages &&
+                                     !(TM == kTreeChunk && ch + hh == tree_ch);
+                            pids[k] = use[k] ? bt[lp] : -1;
+                        }
+                    }
                     int ys[8];
                     int rows[8];
                     int nl = 0;
                     int tree_half = -1;  // half of the block holding the tree chunk
-                    for (int hh = 0; hh < nh; ++hh) {
-                        if (TM == kTreeChunk && ch + hh == tree_ch) {
-                            tree_half = hh;
-                            continue;
-                        }
-                        for (int i = 0; i < nsub; ++i) {
-                            const int tok = (ch + hh) * kChunk + i * Pb;
-                            const int lp = tok / a.P;
-                            if (lp >= npages) break;
-                            const int pid = bt[lp];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (TM == kTreeChunk && hh < nh && ch + hh == tree_ch) tree_half = hh;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int k = hh * 4 + i;
+                            if (!use[k]) continue;
+                            const int pid = pids[k];
                             if (pid < 0 || pid >= a.num_pages) {
                                 report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
                                 continue;
                             }
-                            ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok % a.P);
+                            const int tok = (ch + hh) * kChunk + i * Pb;
+                            ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok & (a.P - 1));
                             rows[nl] = hh * kChunk + i * Pb;
                             ++nl;
                         }
@@ -607,7 +642,7 @@ __global__ void __launch_bounds__(192, 1)
             const bool row_ok = lr < Mrb;
             const bool warp_any = (warp * 32) % R < Mrb;
             bool bad;
-            const int L = clamp_seq_len(a.seq_lens[cur.b], a.P, a.max_pages, bad);
+            const int L = clamp_seq_len(cur.len_raw, a.P, a.max_pages, bad);
             const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
             // Ancestor bits of this row's tree node (tree modes): given, or
             // built here from the parent array by this warp (pointer
@@ -626,7 +661,7 @@ __global__ void __launch_bounds__(192, 1)
                     const bool writer =
                         warp == 0 && cur.unit == cur.b * upb &&
                         cur.chunk_end ==
-                            unit_chunks(a.seq_lens[cur.b], a.P, a.max_pages, TM, a.T, bad_l) &&
+                            unit_chunks(cur.len_raw, a.P, a.max_pages, TM, a.T, bad_l) &&
                         (a.parents_stride != 0 || cur.b == 0);
                     if (writer && bad_tree && lane == 0)
                         report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
@@ -888,16 +923,21 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t to = lane_base + S::TM_O;
             const float acc_scale =
                 (l_err != 0.f && l_sum + l_err > 0.f) ? l_sum / (l_sum + l_err) : 1.f;
-            if (F > 1 && !have_next) {
+            if (!have_next) {
                 // Last segment of this CTA: every MMA and copy has completed,
-                // so the K/V ring is free.  Fold the F row copies into copy 0
-                // through it (rows padded to D + 4 floats, conflict-free), so
-                // the merge reads one partial per CTA instead of F.
+                // so the K/V ring is free.  Each row copy stages its O (scaled
+                // by its own rounding correction) and (m, l) there, rows
+                // padded to D + 4 floats (conflict-free).  Then the four warps
+                // fold the F copies of each query row into one partial, so the
+                // merge reads one partial per CTA instead of F, and store it a
+                // whole row per warp instruction: stored straight from TMEM,
+                // one row per thread, each instruction would touch 32 rows.
                 constexpr int RS = D + 4;
-                float* stg = reinterpret_cast<float*>(smem + S::OFF_STAGE);  // [F-1][R][RS]
-                float* stg_ml = stg + (F - 1) * R * RS;                       // [F-1][R][2]
-                if (g >= 1 && warp_any) {
-                    float* dst = stg + static_cast<size_t>((g - 1) * R + lr) * RS;
+                constexpr int VE = D / 32;                                    // floats per lane
+                float* stg = reinterpret_cast<float*>(smem + S::OFF_STAGE);  // [F][R][RS]
+                float* stg_ml = stg + F * R * RS;                             // [F][R][2]
+                if (warp_any) {
+                    float* dst = stg + static_cast<size_t>(g * R + lr) * RS;
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         float o[32];
@@ -912,61 +952,79 @@ __global__ void __launch_bounds__(192, 1)
                         }
                     }
                     if (row_ok) {
-                        stg_ml[((g - 1) * R + lr) * 2] = m_ref;
-                        stg_ml[((g - 1) * R + lr) * 2 + 1] = l_sum;
+                        stg_ml[(g * R + lr) * 2] = m_ref;
+                        stg_ml[(g * R + lr) * 2 + 1] = l_sum;
                     }
                 }
                 named_bar_sync(1, 128);
-                if (g == 0 && warp_any) {
-                    float mg[F], wg[F];
-                    mg[0] = m_ref;
-                    float mx = m_ref, lc = 0.f;
+                // RU rows per warp at a time: their shared-memory reads are
+                // all issued before any is used.
+                constexpr int RU = 4 / F;
+                for (int q0 = warp; q0 < Mrb; q0 += 4 * RU) {
+                    float mg[RU][F], lg[RU][F], x[RU][F][VE];
 #pragma unroll
-                    for (int k = 1; k < F; ++k) {
-                        mg[k] = row_ok ? stg_ml[((k - 1) * R + lr) * 2] : kNegInf;
-                        mx = fmaxf(mx, mg[k]);
-                    }
+                    for (int u = 0; u < RU; ++u) {
+                        const int q = q0 + 4 * u;
 #pragma unroll
-                    for (int k = 0; k < F; ++k) {
-                        wg[k] = (mg[k] == kNegInf) ? 0.f : ptx::ex2(mg[k] - mx);
-                        lc += wg[k] * (k == 0 ? l_sum
-                                              : (row_ok ? stg_ml[((k - 1) * R + lr) * 2 + 1] : 0.f));
-                    }
-                    float4* acc =
-                        reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
+                        for (int k = 0; k < F; ++k) {
+                            mg[u][k] = kNegInf;
+                            lg[u][k] = 0.f;
 #pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        float o[32];
-                        ptx::tmem_ld32(to + c, o);
-                        ptx::tmem_wait_ld();
-                        if (row_ok) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= wg[0] * acc_scale;
-#pragma unroll
-                            for (int k = 1; k < F; ++k) {
+                            for (int e = 0; e < VE; ++e) x[u][k][e] = 0.f;
+                            if (q < Mrb) {
+                                mg[u][k] = stg_ml[(k * R + q) * 2];
+                                lg[u][k] = stg_ml[(k * R + q) * 2 + 1];
                                 const float* src =
-                                    stg + static_cast<size_t>((k - 1) * R + lr) * RS + c;
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float4 x = *reinterpret_cast<const float4*>(src + 4 * i);
-                                    o[4 * i] = fmaf(wg[k], x.x, o[4 * i]);
-                                    o[4 * i + 1] = fmaf(wg[k], x.y, o[4 * i + 1]);
-                                    o[4 * i + 2] = fmaf(wg[k], x.z, o[4 * i + 2]);
-                                    o[4 * i + 3] = fmaf(wg[k], x.w, o[4 * i + 3]);
+                                    stg + static_cast<size_t>(k * R + q) * RS + lane * VE;
+                                if constexpr (VE == 4) {
+                                    const float4 v4 = *reinterpret_cast<const float4*>(src);
+                                    x[u][k][0] = v4.x;
+                                    x[u][k][1] = v4.y;
+                                    x[u][k][2] = v4.z;
+                                    x[u][k][3] = v4.w;
+                                } else {
+                                    const float2 v2 = *reinterpret_cast<const float2*>(src);
+                                    x[u][k][0] = v2.x;
+                                    x[u][k][1] = v2.y;
                                 }
                             }
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc[c / 4 + i] =
-                                    make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                         }
                     }
-                    if (row_ok) {
-                        slot[r] = mx;
-                        slot[kRows + r] = lc;
+#pragma unroll
+                    for (int u = 0; u < RU; ++u) {
+                        const int q = q0 + 4 * u;
+                        if (q >= Mrb) break;
+                        float mx = kNegInf;
+#pragma unroll
+                        for (int k = 0; k < F; ++k) mx = fmaxf(mx, mg[u][k]);
+                        float lc = 0.f;
+                        float o[VE];
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) o[e] = 0.f;
+#pragma unroll
+                        for (int k = 0; k < F; ++k) {
+                            const float wk =
+                                (mg[u][k] == kNegInf) ? 0.f : ptx::ex2(mg[u][k] - mx);
+                            lc = fmaf(wk, lg[u][k], lc);
+#pragma unroll
+                            for (int e = 0; e < VE; ++e) o[e] = fmaf(wk, x[u][k][e], o[e]);
+                        }
+                        float* acc = slot + 2 * kRows + static_cast<size_t>(q) * D + lane * VE;
+                        if constexpr (VE == 4) {
+                            *reinterpret_cast<float4*>(acc) = make_float4(o[0], o[1], o[2], o[3]);
+                        } else {
+                            *reinterpret_cast<float2*>(acc) = make_float2(o[0], o[1]);
+                        }
+                        if (lane == 0) {
+                            slot[q] = mx;
+                            slot[kRows + q] = lc;
+                        }
                     }
                 }
             } else if (warp_any) {
+                // A later segment follows: the ring holds its K/V, so each row
+                // stores its own partial (hidden behind the next segment's
+                // loads, which are already in flight).
                 float4* acc =
                     reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
 #pragma unroll
@@ -975,7 +1033,7 @@ __global__ void __launch_bounds__(192, 1)
                     ptx::tmem_ld32(to + c, o);
                     ptx::tmem_wait_ld();
                     if (row_ok) {
-                        if constexpr (DENSE) {
+                        if (acc_scale != 1.f) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] *= acc_scale;
                         }
@@ -1094,9 +1152,14 @@ constexpr int kMergeWarps = 4;  // warps per CTA
 // partials (virtual slot v goes to warp v % wpr) and combine through shared
 // memory.  Every independent load of a phase is issued before any of its
 // results is used, so each phase costs about one memory round trip.
-template <int D, int F>
+// SUFFIX: the two-pass form (the tree keys are attended here); otherwise the
+// tree rode on the prefix pass's work line and this is the merge alone.
+template <int D, int F, bool SUFFIX>
 __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const MergeArgs a) {
     constexpr int E = D / 32;
+    // Accumulator rows each warp loads in the first round trip, together
+    // with the (m, l) of its partials.
+    constexpr int NF = 4;
     constexpr int R = kRows / F;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1127,7 +1190,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
 
     // Parent array of this row's tree (masks built here): lane l holds the
     // parents of nodes l and l + 32.  Loaded now, used after the plan.
-    const bool suffix_here = a.tmode == kTreeNone;
+    constexpr bool suffix_here = SUFFIX;
     int par0 = -1, par1 = -1;
     if (suffix_here && a.parents != nullptr && sub == 0) {
         const int32_t* pr = a.parents + static_cast<size_t>(b) * a.parents_stride;
@@ -1136,25 +1199,37 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     }
 
     // ---- work-line plan of this unit (inputs only): sequence lengths of
-    // the whole batch, loaded 64 at a time.
+    // the whole batch, the first 32 * kPlanRegs and this unit's own loaded in
+    // one round trip.
     const int upb = a.Hkv * a.RB;
+    int32_t lraw[kPlanRegs];
+#pragma unroll
+    for (int i = 0; i < kPlanRegs; ++i) {
+        const int bi = 32 * i + lane;
+        lraw[i] = bi < a.B ? a.seq_lens[bi] : 0;
+    }
+    const int32_t l_own = a.seq_lens[b];
     long long W = 0, base_b = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 64) {
-        const int b1 = b0 + lane, b2 = b0 + 32 + lane;
-        const int32_t l1 = b1 < a.B ? a.seq_lens[b1] : 0;
-        const int32_t l2 = b2 < a.B ? a.seq_lens[b2] : 0;
-        bool bad;
-        const int n1 =
-            b1 < a.B ? unit_len(unit_chunks(l1, a.P, a.max_pages, a.tmode, a.T, bad), a.ovh) : 0;
-        const int n2 =
-            b2 < a.B ? unit_len(unit_chunks(l2, a.P, a.max_pages, a.tmode, a.T, bad), a.ovh) : 0;
-        W += __reduce_add_sync(kFull, n1 + n2);
-        base_b += __reduce_add_sync(kFull, (b1 < b ? n1 : 0) + (b2 < b ? n2 : 0));
+    auto add_len = [&](int bi, int32_t L_raw) {
+        bool bad_i;
+        const int n =
+            bi < a.B ? unit_len(unit_chunks(L_raw, a.P, a.max_pages, a.tmode, a.T, bad_i), a.ovh)
+                     : 0;
+        W += __reduce_add_sync(kFull, n);
+        base_b += __reduce_add_sync(kFull, bi < b ? n : 0);
+    };
+#pragma unroll
+    for (int i = 0; i < kPlanRegs; ++i)
+        if (32 * i < a.B) add_len(32 * i + lane, lraw[i]);
+#pragma unroll 1
+    for (int b0 = 32 * kPlanRegs; b0 < a.B; b0 += 32) {
+        const int bi = b0 + lane;
+        add_len(bi, bi < a.B ? a.seq_lens[bi] : 0);
     }
     W *= upb;
     base_b *= upb;
     bool bad;
-    const int nch = unit_chunks(a.seq_lens[b], a.P, a.max_pages, a.tmode, a.T, bad);
+    const int nch = unit_chunks(l_own, a.P, a.max_pages, a.tmode, a.T, bad);
     int c_first = 0, c_last = -1;
     // A prefix CTA folds its F row copies into one partial in its last
     // segment.  Every CTA before c_last ends inside this unit; c_last does
@@ -1218,7 +1293,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         int L_b = 0;
         if (a.tree_in_cache) {
             bool bad_len;
-            L_b = clamp_seq_len(a.seq_lens[b], a.P, a.max_pages, bad_len);
+            L_b = clamp_seq_len(l_own, a.P, a.max_pages, bad_len);
         }
         while (bits != 0) {
             int js[4];
@@ -1331,16 +1406,19 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     // k-th) and the accumulator rows of its first four.  Partials are read
     // through L2 only (ld.global.cg): the prefix grid wrote them while this
     // grid was resident.
+    // Bit k: the warp's k-th partial exists (one work check per lane, not
+    // one per unrolled load below).
+    const unsigned have = __ballot_sync(kFull, lane < nmine && v_work(v_of(lane)));
     float m_j = kNegInf, l_j = 0.f;
-    if (lane < nmine && v_work(v_of(lane))) {
+    if ((have >> lane) & 1u) {
         m_j = __ldcg(a.ws + v_m(v_of(lane)));
         l_j = __ldcg(a.ws + v_m(v_of(lane)) + kRows);
     }
-    float v[4][E];
+    float v[NF][E];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        load_acc<E>(a.ws + v_acc(v_of(j)), j < nmine && v_work(v_of(j)), v[j]);
+    for (int j = 0; j < NF; ++j) load_acc<E>(a.ws + v_acc(v_of(j)), (have >> j) & 1u, v[j]);
     float mx = fmaxf(m_s, m_j);
+#pragma unroll 1
     for (int k = 32 + lane; k < nmine; k += 32)  // rare: more than 32 partials per warp
         if (v_work(v_of(k))) mx = fmaxf(mx, __ldcg(a.ws + v_m(v_of(k))));
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
@@ -1357,12 +1435,13 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     float wc = (m_j == kNegInf || !has_keys) ? 0.f : ptx::ex2(m_j - mx);
     float total = l_s * w_s + warp_sum(wc * l_j);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NF; ++j) {
         const float wj = __shfl_sync(kFull, wc, j);
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
     }
     // Remaining partials of this warp, four accumulator rows per round trip.
+#pragma unroll 1
     for (int k0 = 0; k0 < nmine; k0 += 32) {
         if (k0 != 0) {
             const int k = k0 + lane;
@@ -1376,7 +1455,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
             total += warp_sum(wc * lc);
         }
         const int nb = min(32, nmine - k0);
-        for (int j0 = (k0 == 0) ? 4 : 0; j0 < nb; j0 += 4) {
+#pragma unroll 1
+        for (int j0 = (k0 == 0) ? NF : 0; j0 < nb; j0 += 4) {
             float wj[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -1550,8 +1630,13 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     const int rows = M < kRows ? M : kRows;
     const int rows_per_cta = kMergeWarps / ma.wpr;
     const dim3 grid(static_cast<unsigned>(units), (rows + rows_per_cta - 1) / rows_per_cta);
-    auto kernel = F == 4 ? suffix_merge_kernel<D, 4>
-                         : (F == 2 ? suffix_merge_kernel<D, 2> : suffix_merge_kernel<D, 1>);
+    using K = void (*)(MergeArgs);
+    const K table[2][3] = {
+        {suffix_merge_kernel<D, 1, false>, suffix_merge_kernel<D, 2, false>,
+         suffix_merge_kernel<D, 4, false>},
+        {suffix_merge_kernel<D, 1, true>, suffix_merge_kernel<D, 2, true>,
+         suffix_merge_kernel<D, 4, true>}};
+    const K kernel = table[v.tmode == kTreeNone ? 1 : 0][F == 4 ? 2 : (F == 2 ? 1 : 0)];
     return launch_pdl(kernel, grid, dim3(32 * kMergeWarps), 0, stream, ma);
 }
 

@@ -118,13 +118,34 @@ TA_HD int unit_chunks(int32_t L_raw, int P, int max_pages, int tmode, int T, boo
     return chunks_of(L);
 }
 
+// n / d for n >= 0, d > 0.  When both fit in 32 bits (every realistic call)
+// the quotient comes from one 32-bit unsigned division: on the GPU a 64-bit
+// division is a long dependent instruction sequence, and these divisions sit
+// on the path from kernel start to the first KV load.  Exact either way.
+#if defined(__CUDACC__)
+// Out of line on the GPU: one copy of the 64-bit division per kernel instead
+// of one inlined at every call site (the inlined sequence is long, and code
+// size is latency for kernels that run through their code once per launch).
+static __host__ __device__ __noinline__ long long div_nn_wide(long long n, long long d) {
+    return n / d;
+}
+#else
+inline long long div_nn_wide(long long n, long long d) { return n / d; }
+#endif
+
+TA_HD long long div_nn(long long n, long long d) {
+    if (((n | d) >> 32) == 0)
+        return static_cast<long long>(static_cast<uint32_t>(n) / static_cast<uint32_t>(d));
+    return div_nn_wide(n, d);
+}
+
 TA_HD long long cta_start(int c, long long W, int C) {
-    return static_cast<long long>(c) * W / C;
+    return div_nn(static_cast<long long>(c) * W, C);
 }
 
 // The CTA whose range holds work-line position x (0 <= x < W).
 TA_HD int cta_of(long long x, long long W, int C) {
-    return static_cast<int>((x * C + C - 1) / W);
+    return static_cast<int>(div_nn(x * C + C - 1, W));
 }
 
 // True when CTA c has work (an empty range happens when W < C).  The merge
@@ -143,6 +164,7 @@ TA_HD int unit_len(int nch, int ovh) { return nch > 0 ? nch + ovh : 0; }
 struct Segment {
     int b, hk, rb, unit;
     int chunk_begin, chunk_end;  // chunk indices within sequence b
+    int32_t len_raw;             // seq_lens[b] as read (not clamped)
 };
 
 // Walks the segments of one CTA's range in order.  `seq_lens` is read
@@ -156,11 +178,13 @@ struct Walker {
     long long base;  // work-line position of sequence b's first unit
     int nch;         // chunks per unit of sequence b
     int len;         // work-line length per unit of sequence b
+    int32_t lraw;    // seq_lens[b], read once per sequence
     long long x, x1; // current position and end of this CTA's range
 
-    TA_HD int chunks_b(int bb) const {
+    TA_HD int chunks_b(int bb) {
         bool bad;
-        return unit_chunks(seq_lens[bb], P, max_pages, tmode, T, bad);
+        lraw = seq_lens[bb];
+        return unit_chunks(lraw, P, max_pages, tmode, T, bad);
     }
 
     TA_HD void init(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
@@ -179,6 +203,7 @@ struct Walker {
         base = base0;
         x = x0;
         x1 = x1_;
+        lraw = 0;
         nch = (x0 < x1_) ? chunks_b(b0) : 0;
         len = unit_len(nch, ovh);
     }
@@ -192,8 +217,8 @@ struct Walker {
                 len = unit_len(nch, ovh);
             }
             const long long off = x - base;
-            const int urel = static_cast<int>(off / len);
-            const int pos = static_cast<int>(off % len);
+            const int urel = static_cast<int>(div_nn(off, len));
+            const int pos = static_cast<int>(off - static_cast<long long>(urel) * len);
             const long long ubase = base + static_cast<long long>(urel) * len;
             if (pos >= nch) {  // the unit's overhead slots: no chunks
                 x = ubase + len;
@@ -207,6 +232,7 @@ struct Walker {
             s.unit = b * units_per_b + urel;
             s.chunk_begin = pos;
             s.chunk_end = pos + static_cast<int>(e - x);
+            s.len_raw = lraw;
             x = e;
             return true;
         }

@@ -9,7 +9,9 @@
 //     (one folded partial per CTA before the unit's last CTA, then the last
 //     CTA's one folded or F unfolded copies) are exactly those written: a
 //     prefix CTA folds its copies in its last segment only,
-//   * the descriptor helpers put each field where the bit layout says.
+//   * the descriptor helpers put each field where the bit layout says,
+//   * the division helper matches plain 64-bit division on both of its
+//     paths, and cta_of inverts cta_start on work lines longer than 2^32.
 // Prints "OK" and exits 0, or prints the first failure and exits 1.
 #include <cstdio>
 #include <cstdlib>
@@ -60,6 +62,7 @@ static bool check_partition(int B, int Hkv, int RB, int P, int maxp, int C, int 
             segs.push_back(s);
             CHECK(s.chunk_end > s.chunk_begin, "empty segment");
             CHECK(s.unit == (s.b * Hkv + s.hk) * RB + s.rb, "unit index");
+            CHECK(s.len_raw == sl[s.b], "segment's cached sequence length");
             bool bad;
             const int nch = unit_chunks(sl[s.b], P, maxp, tmode, T, bad);
             CHECK(s.chunk_end <= nch, "segment past the sequence");
@@ -144,8 +147,34 @@ static bool check_descriptors() {
     return true;
 }
 
+static bool check_division() {
+    for (int i = 0; i < 200000; ++i) {
+        const unsigned long long hi = next_rand(), lo = next_rand();
+        long long n = static_cast<long long>(((hi << 32) | lo) >> (next_rand() % 64));
+        if (n < 0) n = -(n + 1);
+        long long d = static_cast<long long>(next_rand() >> (next_rand() % 31)) + 1;
+        if (i % 3 == 0) d = (d << (next_rand() % 32)) + 1;
+        CHECK(div_nn(n, d) == n / d, "div_nn(%lld, %lld)", n, d);
+    }
+    // Work lines whose c * W or x * C leave 32 bits.
+    for (int i = 0; i < 2000; ++i) {
+        const int C = 1 + next_rand() % 300;
+        const long long W =
+            1 + ((static_cast<long long>(next_rand()) << (next_rand() % 24)) | next_rand());
+        const int c = next_rand() % C;
+        const long long a = cta_start(c, W, C), b = cta_start(c + 1, W, C);
+        CHECK(a == static_cast<long long>(c) * W / C, "cta_start");
+        if (a < b) {
+            CHECK(cta_of(a, W, C) == c, "cta_of(start) W=%lld C=%d c=%d", W, C, c);
+            CHECK(cta_of(b - 1, W, C) == c, "cta_of(end - 1) W=%lld C=%d c=%d", W, C, c);
+        }
+    }
+    return true;
+}
+
 int main() {
     if (!check_descriptors()) return 1;
+    if (!check_division()) return 1;
     const int Ps[4] = {16, 32, 64, 128};
     for (int trial = 0; trial < 400; ++trial) {
         const int B = 1 + next_rand() % 9;
