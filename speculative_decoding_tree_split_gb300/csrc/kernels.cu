@@ -216,6 +216,8 @@ __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
     return v;
 }
 
+constexpr int kL1Line = 128;  // bytes per L1 cache line
+
 // Sequences whose work-line lengths the plan keeps in registers (32 per
 // entry): their seq_lens are read in one round trip, all loads in flight.
 constexpr int kPlanRegs = 4;
@@ -352,9 +354,22 @@ __global__ void __launch_bounds__(192, 1)
         ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), S::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // L2 policy of the K/V loads (reads no input, so it is made before the wait).
+    const uint64_t pol = (warp == 4 && lane == 0) ? ptx::policy_evict_first() : 0ull;
     // Inputs may come from the kernel before us in the stream.
     ptx::grid_dep_wait();
     if (warp == 0) compute_plan(a, lane, misc);
+    if (warp == 4) {
+        // A small block table is pulled into L1 while the plan is computed, so
+        // the producer's first page lookups do not each wait for L2.
+        const long long lines =
+            (static_cast<long long>(a.B) * a.max_pages * 4 + kL1Line - 1) / kL1Line;
+        if (lines <= 2 * 32) {
+            const char* bt = reinterpret_cast<const char*>(a.block_table);
+            if (lane < lines) ptx::prefetch_l1(bt + static_cast<size_t>(lane) * kL1Line);
+            if (lane + 32 < lines) ptx::prefetch_l1(bt + static_cast<size_t>(lane + 32) * kL1Line);
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -373,7 +388,6 @@ __global__ void __launch_bounds__(192, 1)
             Walker w;
             w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
                    misc->x1, TM, a.T, a.ovh);
-            const uint64_t pol = ptx::policy_evict_first();
             const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
             const int nsub = kChunk / Pb;                // boxes per 64-token step
             const int pshift = __ffs(a.P) - 1;           // page_size is a power of two
@@ -389,6 +403,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (TM == kTreeInCache) npages = min(a.max_pages, (L + a.T + a.P - 1) / a.P);
                 const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
                 const int32_t* bt = a.block_table + static_cast<size_t>(sg.b) * a.max_pages;
+#pragma unroll 1
                 for (int ch = sg.chunk_begin; ch < sg.chunk_end; ch += 2, ++jj) {
                     const int nh = min(2, sg.chunk_end - ch);  // 64-token steps in this block
                     const int s = jj % S::NS;
@@ -452,6 +467,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
                     const uint32_t vst = kst + S::TILE_BYTES;
+#pragma unroll 1
                     for (int l = 0; l < nl; ++l) {
 #pragma unroll
                         for (int h = 0; h < S::DH; ++h) {
@@ -922,7 +938,7 @@ __global__ void __launch_bounds__(192, 1)
             float* slot = a.ws + static_cast<size_t>(cur.unit + blockIdx.x) * slot_floats(D);
             const uint32_t to = lane_base + S::TM_O;
             const float acc_scale =
-                (l_err != 0.f && l_sum + l_err > 0.f) ? l_sum / (l_sum + l_err) : 1.f;
+                (l_err != 0.f && l_sum + l_err > 0.f) ? __fdividef(l_sum, l_sum + l_err) : 1.f;
             if (!have_next) {
                 // Last segment of this CTA: every MMA and copy has completed,
                 // so the K/V ring is free.  Each row copy stages its O (scaled
@@ -1491,7 +1507,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         if (lane == 0) *lp = kNegInf;
         return;
     }
-    const float inv = 1.f / total;
+    const float inv = __fdividef(1.f, total);
     if constexpr (E == 4) {
         uint2 pk;
         pk.x = pack_bf16(o[0] * inv, o[1] * inv);
