@@ -533,8 +533,14 @@ __global__ void __launch_bounds__(192, 1)
                             const uint32_t vst =
                                 sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
                             const uint32_t pt = tmem + S::TM_P + (j & 1) * (kBlock / 2);
+                            // A block of one 64-token step has no keys in its
+                            // second half (P is zero there): half the MMAs.
+                            const int nk = sg.chunk_end - sg.chunk_begin - 2 * np >= 2
+                                               ? kBlock / 16
+                                               : kChunk / 16;
 #pragma unroll
                             for (int k = 0; k < kBlock / 16; ++k) {
+                                if (k >= nk) break;
                                 const uint64_t bd =
                                     smem_desc_sw128(vst + k * 16 * 128, S::HALF_BYTES, 1024);
                                 ptx::mma_bf16_ts(tmem + S::TM_O, pt + k * 8, bd, idesc_pv,
