@@ -313,9 +313,19 @@ TA_HD int overhead_slots(int F, int M) {
     return o > 8 ? 8 : o;
 }
 
-// Work-line steps per CTA at or below which the tree tokens ride on the
-// prefix pass (a call this small is latency-bound, and the merge's own tree
-// pass sits on its critical path); above it the merge kernel attends them.
+// Where the tree tokens go.  They ride on the prefix pass (one extra step per
+// unit) when
+//   * the call has at most kTreeInPrefixMaxSteps work-line steps per CTA: it
+//     is latency-bound, and the merge's own tree pass sits on its critical
+//     path; or
+//   * there are no more units than CTAs and the tile holds at least two row
+//     copies: the extra steps then cost at most one block per CTA, less than
+//     the merge's tree pass over every query row.  (With one row copy the
+//     tree-mode softmax spills registers; with more units than CTAs the extra
+//     blocks outweigh the merge's work.  Measured on GB300: Llama-3.1-70B layer
+//     73.1 -> 69.6 us with the tree on the prefix pass, the B=64 chain
+//     360.5 -> 369.2 us and the Maverick layer 96.6 -> 105.1 us.)
+// Otherwise the merge kernel attends them.
 constexpr int kTreeInPrefixMaxSteps = 32;
 
 // tree_layout: kTreeNone for the prefix pass alone (two-pass API), else where
@@ -340,10 +350,10 @@ TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm
         return sm_count < cap ? sm_count : static_cast<int>(cap);
     };
     p.tmode = kTreeNone;
-    if (tree_layout != kTreeNone &&
-        prefix_steps <= static_cast<long long>(kTreeInPrefixMaxSteps) *
-                            ctas_for(prefix_steps + p.units))
-        p.tmode = tree_layout;
+    const int C = ctas_for(prefix_steps + p.units);
+    const bool small_call = prefix_steps <= static_cast<long long>(kTreeInPrefixMaxSteps) * C;
+    const bool few_units = p.units <= C && p.F >= 2;
+    if (tree_layout != kTreeNone && (small_call || few_units)) p.tmode = tree_layout;
     p.ovh = overhead_slots(p.F, p.M);
     p.max_steps = prefix_steps + (p.tmode == kTreeChunk ? p.units : 0);
     p.n_ctas = ctas_for(p.max_steps);

@@ -369,12 +369,13 @@ def test_both_tree_placements(oracle, n_ctas):
 
 @pytest.mark.parametrize("per_seq", [False, True], ids=["shared", "per_seq"])
 def test_verify_tree_two_pass_form(oracle, per_seq):
-    # 16 x 8 units x 64 steps is more than 32 steps per CTA on any GB300, so
-    # the merge kernel attends the tree (masks built there from the parents)
-    cfg = Config("vt2", B=16, Hq=32, Hkv=8, d=128, L=4096, page=64, T=8, max_depth=3,
+    # 24 x 8 = 192 units (more than GB300's 152 SMs) x 64 steps is more than
+    # 32 steps per CTA, so the merge kernel attends the tree (masks built
+    # there from the parents)
+    cfg = Config("vt2", B=24, Hq=32, Hkv=8, d=128, L=4096, page=64, T=8, max_depth=3,
                  max_branch=3, seed=95)
     wl = make_workload(cfg, per_sequence_trees=per_seq)
-    p = ta.plan(16, 32, 8, 128, 8, 64, wl.max_pages_per_seq)
+    p = ta.plan(24, 32, 8, 128, 8, 64, wl.max_pages_per_seq)
     assert p["tree_in_prefix"] == 0
     x = to_dev(wl)
     mask = ta.mask_build_batched(x["parents"]) if per_seq else ta.mask_build(x["parents"])

@@ -32,10 +32,15 @@ EXPECTED = {
 
 def test_plan_tree_placement_by_hand():
     # llama8b: 8 units x 128 steps = 1024 <= 32 x 152 -> tree on the prefix pass;
-    # llama70b: 128 units x 128 = 16384 > 4864 -> the merge attends the tree
-    c = CONFIGS["llama8b"]
-    assert ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)["tree_in_prefix"] == 1
-    for name in ("llama70b", "chain", "maverick"):
+    # llama70b: 128 units x 128 = 16384 > 4864 steps, but 128 units <= 152 CTAs
+    # with 2 row copies -> tree on the prefix pass;
+    # chain: 512 units > 152 CTAs; maverick: one row copy (M = 80) -> the merge
+    # attends the tree
+    for name in ("llama8b", "llama70b"):
+        c = CONFIGS[name]
+        p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+        assert p["tree_in_prefix"] == 1, name
+    for name in ("chain", "maverick"):
         c = CONFIGS[name]
         p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
         assert p["tree_in_prefix"] == 0, name
@@ -74,9 +79,11 @@ def test_plan_invariants(B, Hq, Hkv, d, T, P, maxp):
     assert p["row_blocks"] == (M + 127) // 128
     assert p["units"] == B * Hkv * p["row_blocks"]
     prefix_steps = p["units"] * ((maxp * P + 63) // 64)
-    # small calls (<= 32 steps per CTA) attend the tree in the prefix pass,
+    # small calls (<= 32 steps per CTA), and calls with no more units than
+    # CTAs and at least two row copies, attend the tree in the prefix pass:
     # one extra 64-key chunk per unit
-    want_tree = prefix_steps <= 32 * min(SMS, prefix_steps + p["units"])
+    C = min(SMS, prefix_steps + p["units"])
+    want_tree = prefix_steps <= 32 * C or (p["units"] <= C and p["replicas"] >= 2)
     assert p["tree_in_prefix"] == int(want_tree)
     assert p["max_steps"] == prefix_steps + (p["units"] if want_tree else 0)
     assert 1 <= p["n_ctas"] <= min(SMS, max(1, p["max_steps"]))
