@@ -289,6 +289,38 @@ def test_full_size_configs(oracle, name):
     assert np.abs(got_l - ref_l).max() <= LSE_TOL
 
 
+@pytest.mark.parametrize("name", ["llama8b", "llama70b", "chain", "maverick"])
+def test_full_size_verify_tree(oracle, name):
+    # The call bench.py times: masks built from the parent array inside the
+    # call, at each workload's full size, with the kernel selector's own tree
+    # placement (prefix pass for llama8b and llama70b, merge kernel for the
+    # chain and Maverick); sampled rows against the oracle.
+    cfg = CONFIGS[name]
+    wl = make_workload(cfg)
+    x = to_dev(wl)
+    B, T = cfg.B, cfg.T
+    p = ta.plan(B, cfg.Hq, cfg.Hkv, cfg.d, T, cfg.page, wl.max_pages_per_seq)
+    assert p["tree_in_prefix"] == (1 if name in ("llama8b", "llama70b") else 0)
+    mask_out = torch.zeros(T, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                              x["seq_lens"], x["tree_k"], x["tree_v"], x["parents"],
+                              mask_out=mask_out, status=status, softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    want_mask = oracle.tree_mask(wl.parents.tolist())
+    assert np.array_equal(mask_out.cpu().numpy().view(np.uint64), want_mask)
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rows = sample_rows(cfg, 96, cfg.seed + 1)
+    ref_o, ref_l = oracle.verify_rows(wl, want_mask, rows)
+    got_o = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    got_l = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert np.abs(got_o - ref_o).max() <= OUT_TOL
+    assert np.abs(got_l - ref_l).max() <= LSE_TOL
+
+
 @pytest.mark.parametrize("T,G,n_ctas", [(4, 4, 2), (8, 4, 3), (12, 4, 2), (16, 4, 2), (20, 4, 1),
                                         (16, 5, 2)])
 def test_row_replication_paths(oracle, T, G, n_ctas):
