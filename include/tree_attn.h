@@ -363,6 +363,9 @@ typedef struct tree_attn_plan_info {
     int tree_in_prefix;      /* 1: the prefix pass attends the tree tokens too (one   */
                              /* masked chunk per unit; small, latency-bound calls);   */
                              /* 0: the suffix/merge kernel attends them               */
+    int merge_rows_per_warp; /* query rows each merge warp takes in turn (> 1 only    */
+                             /* when the tree is on the prefix pass and one row per   */
+                             /* warp would need more merge CTAs than the SMs hold)    */
 } tree_attn_plan_info;
 
 TREE_ATTN_API int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size,

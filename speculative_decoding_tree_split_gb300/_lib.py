@@ -63,7 +63,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("units", ctypes.c_int), ("row_blocks", ctypes.c_int),
                 ("replicas", ctypes.c_int), ("n_ctas", ctypes.c_int),
                 ("merge_warps_per_row", ctypes.c_int), ("max_steps", ctypes.c_longlong),
-                ("workspace_bytes", ctypes.c_size_t), ("tree_in_prefix", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_size_t), ("tree_in_prefix", ctypes.c_int),
+                ("merge_rows_per_warp", ctypes.c_int)]
 
 
 class TreeAttnError(RuntimeError):

@@ -1234,6 +1234,7 @@ struct MergeArgs {
     float* lse;
     int B, Hq, Hkv, G, T, M, RB, P, max_pages, n_ctas;
     int wpr;  // warps per query row in the merge (1, 2, 4 or 8)
+    int rpw;  // rows per warp (taken in turn; merge without the tree pass only)
     float scale_log2;
     int mask_stride;  // 0: one tree for the batch; T: tree b at mask[b * T]
     // Tree tokens padded inside the paged cache (tree_k / tree_v unused):
@@ -1298,7 +1299,6 @@ __device__ __forceinline__ void load_acc(const float* p, bool use, float* v) {
     }
 }
 
-constexpr int kMergeWarps = 4;  // warps per CTA
 
 // One CTA = 4 warps = 4 / wpr query rows; the wpr warps of a row split its
 // partials (virtual slot v goes to warp v % wpr) and combine through shared
@@ -1306,8 +1306,10 @@ constexpr int kMergeWarps = 4;  // warps per CTA
 // results is used, so each phase costs about one memory round trip.
 // SUFFIX: the two-pass form (the tree keys are attended here); otherwise the
 // tree rode on the prefix pass's work line and this is the merge alone.
-template <int D, int F, bool SUFFIX>
-__global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const MergeArgs a) {
+// MULTI: each warp takes a.rpw rows in turn (merge alone only).
+template <int D, int F, bool SUFFIX, bool MULTI>
+__global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
+    suffix_merge_kernel(const MergeArgs a) {
     constexpr int E = D / 32;
     // Accumulator rows each warp loads in the first round trip, together
     // with the (m, l) of its partials.
@@ -1323,9 +1325,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     const int rb = unit % a.RB;
     const int hk = (unit / a.RB) % a.Hkv;
     const int b = unit / (a.RB * a.Hkv);
-    const int r = blockIdx.y * rows_per_cta + wr;
-    const int rr = rb * kRows + r;
-    const bool active = r < kRows && rr < a.M;
     // The next kernel may start its prologue once every CTA of this grid is
     // running; it waits for this grid before reading anything it writes.
     ptx::grid_dep_launch();
@@ -1333,12 +1332,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
     __shared__ float red_m[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
     __shared__ float red_o[kMergeWarps][D];
-
-    int t = 0, h = 0;
-    if (active) {
-        t = rr / a.G;
-        h = hk * a.G + rr % a.G;
-    }
 
     // Parent array of this row's tree (masks built here): lane l holds the
     // parents of nodes l and l + 32.  Loaded now, used after the plan.
@@ -1396,263 +1389,279 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 6) suffix_merge_kernel(const
         if (F > 1) last_folded = cta_start(c_last + 1, W, a.n_ctas) <= ustart + len;
     }
 
-    // ---- suffix (sub-warp 0 of each row): softmax over the tree keys
-    // mask[t] allows, four keys per round trip.  Reads only inputs of this
-    // call, so it runs before waiting for the prefix pass.
-    float m_s = kNegInf, l_s = 0.f;
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    // Tree mask of this row's node: given, or built here from the parent
-    // array -- by walking the parent links up from node t (the row's warp
-    // holds the array in registers: one shuffle per ancestor).  A link that
-    // does not point to an earlier node ends the walk (that node is then a
-    // root, as in tree_mask_kernel, which reports it).
-    uint64_t bits = 0;
-    if (suffix_here && a.parents != nullptr && sub == 0) {
-        for (int node = t, steps = 0; node >= 0 && steps < 64; ++steps) {
-            bits |= 1ull << node;
-            const int n0 = __shfl_sync(kFull, par0, node & 31);
-            const int n1 = __shfl_sync(kFull, par1, node & 31);
-            const int nxt = node < 32 ? n0 : n1;
-            node = (nxt >= -1 && nxt < node) ? nxt : -1;
+    // Each warp takes rpw rows in turn (more than one only for the merge
+    // alone, when one row per warp would need more CTAs than fit at once).
+    static_assert(!(SUFFIX && MULTI), "the tree pass runs one row per warp");
+    const int rpw = MULTI ? a.rpw : 1;
+#pragma unroll 1
+    for (int rep = 0; rep < rpw; ++rep) {
+        const int r = (blockIdx.y * rpw + rep) * rows_per_cta + wr;
+        const int rr = rb * kRows + r;
+        const bool active = r < kRows && rr < a.M;
+        int t = 0, h = 0;
+        if (active) {
+            t = rr / a.G;
+            h = hk * a.G + rr % a.G;
         }
-        // One warp per tree validates the array and writes the masks out:
-        // the first unit's of the sequence (per-sequence trees) or of the
-        // batch (pointer jumping over all nodes, as in tree_mask_kernel).
-        const bool writer = unit == b * upb && blockIdx.y == 0 && warp == 0 &&
-                            (a.parents_stride != 0 || b == 0);
-        uint64_t anc[2] = {0ull, 0ull};
-        bool bad_tree = false;
-        if (writer)
-            bad_tree = warp_tree_mask(a.parents + static_cast<size_t>(b) * a.parents_stride,
-                                      a.T, lane, anc);
-        if (writer && bad_tree && lane == 0) report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
-        if (writer && a.mask_out != nullptr) {
+
+        // ---- suffix (sub-warp 0 of each row): softmax over the tree keys
+        // mask[t] allows, four keys per round trip.  Reads only inputs of this
+        // call, so it runs before waiting for the prefix pass.
+        float m_s = kNegInf, l_s = 0.f;
+        float acc[E];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = lane + 32 * hh;
-                if (i < a.T) a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        // Tree mask of this row's node: given, or built here from the parent
+        // array -- by walking the parent links up from node t (the row's warp
+        // holds the array in registers: one shuffle per ancestor).  A link that
+        // does not point to an earlier node ends the walk (that node is then a
+        // root, as in tree_mask_kernel, which reports it).
+        uint64_t bits = 0;
+        if (suffix_here && a.parents != nullptr && sub == 0) {
+            for (int node = t, steps = 0; node >= 0 && steps < 64; ++steps) {
+                bits |= 1ull << node;
+                const int n0 = __shfl_sync(kFull, par0, node & 31);
+                const int n1 = __shfl_sync(kFull, par1, node & 31);
+                const int nxt = node < 32 ? n0 : n1;
+                node = (nxt >= -1 && nxt < node) ? nxt : -1;
             }
-        }
-    } else if (suffix_here && a.mask != nullptr && active && sub == 0) {
-        bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
-    }
-    if (a.T < 64) bits &= (1ull << a.T) - 1ull;
-    if (suffix_here && active && sub == 0 && (a.mask != nullptr || a.parents != nullptr)) {
-        float qv[E];
-        load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
-        int L_b = 0;
-        if (a.tree_in_cache) {
-            bool bad_len;
-            L_b = clamp_seq_len(l_own, a.P, a.max_pages, bad_len);
-        }
-        while (bits != 0) {
-            int js[4];
-            int n = 0;
+            // One warp per tree validates the array and writes the masks out:
+            // the first unit's of the sequence (per-sequence trees) or of the
+            // batch (pointer jumping over all nodes, as in tree_mask_kernel).
+            const bool writer = unit == b * upb && blockIdx.y == 0 && warp == 0 &&
+                                (a.parents_stride != 0 || b == 0);
+            uint64_t anc[2] = {0ull, 0ull};
+            bool bad_tree = false;
+            if (writer)
+                bad_tree = warp_tree_mask(a.parents + static_cast<size_t>(b) * a.parents_stride,
+                                          a.T, lane, anc);
+            if (writer && bad_tree && lane == 0) report(a.status, TREE_ATTN_STATUS_BAD_PARENT);
+            if (writer && a.mask_out != nullptr) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                js[i] = 0;
-                if (bits != 0) {
-                    js[i] = __ffsll(static_cast<long long>(bits)) - 1;
-                    bits &= bits - 1;
-                    n = i + 1;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int i = lane + 32 * hh;
+                    if (i < a.T) a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
                 }
             }
-            float kv[4][E], vv[4][E];
+        } else if (suffix_here && a.mask != nullptr && active && sub == 0) {
+            bits = a.mask[static_cast<size_t>(b) * a.mask_stride + t];
+        }
+        if (a.T < 64) bits &= (1ull << a.T) - 1ull;
+        if (suffix_here && active && sub == 0 && (a.mask != nullptr || a.parents != nullptr)) {
+            float qv[E];
+            load_bf16<E>(a.q + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E, qv);
+            int L_b = 0;
             if (a.tree_in_cache) {
-                // Position L_b + j of the paged cache (the tree padding).
-                int page[4];
+                bool bad_len;
+                L_b = clamp_seq_len(l_own, a.P, a.max_pages, bad_len);
+            }
+            while (bits != 0) {
+                int js[4];
+                int n = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    page[i] = -1;
-                    const int pos = L_b + js[i];
-                    if (i < n && pos / a.P < a.max_pages)
-                        page[i] = a.block_table[static_cast<size_t>(b) * a.max_pages + pos / a.P];
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (i >= n) continue;
-                    const int pos = L_b + js[i];
-                    if (page[i] < 0 || page[i] >= a.num_pages) {
-                        if (lane == 0)
-                            report(a.status, pos / a.P < a.max_pages ? TREE_ATTN_STATUS_BAD_PAGE
-                                                                     : TREE_ATTN_STATUS_BAD_SEQ_LEN);
-#pragma unroll
-                        for (int e = 0; e < E; ++e) kv[i][e] = vv[i][e] = 0.f;
-                        continue;
+                    js[i] = 0;
+                    if (bits != 0) {
+                        js[i] = __ffsll(static_cast<long long>(bits)) - 1;
+                        bits &= bits - 1;
+                        n = i + 1;
                     }
-                    const size_t off =
-                        ((static_cast<size_t>(page[i]) * a.Hkv + hk) * a.P + pos % a.P) * D +
-                        lane * E;
-                    load_bf16<E>(a.k_pages + off, kv[i]);
-                    load_bf16<E>(a.v_pages + off, vv[i]);
                 }
-            } else {
+                float kv[4][E], vv[4][E];
+                if (a.tree_in_cache) {
+                    // Position L_b + j of the paged cache (the tree padding).
+                    int page[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        page[i] = -1;
+                        const int pos = L_b + js[i];
+                        if (i < n && pos / a.P < a.max_pages)
+                            page[i] = a.block_table[static_cast<size_t>(b) * a.max_pages + pos / a.P];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i >= n) continue;
+                        const int pos = L_b + js[i];
+                        if (page[i] < 0 || page[i] >= a.num_pages) {
+                            if (lane == 0)
+                                report(a.status, pos / a.P < a.max_pages ? TREE_ATTN_STATUS_BAD_PAGE
+                                                                         : TREE_ATTN_STATUS_BAD_SEQ_LEN);
+#pragma unroll
+                            for (int e = 0; e < E; ++e) kv[i][e] = vv[i][e] = 0.f;
+                            continue;
+                        }
+                        const size_t off =
+                            ((static_cast<size_t>(page[i]) * a.Hkv + hk) * a.P + pos % a.P) * D +
+                            lane * E;
+                        load_bf16<E>(a.k_pages + off, kv[i]);
+                        load_bf16<E>(a.v_pages + off, vv[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i < n) {
+                            const size_t off =
+                                ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
+                            load_bf16<E>(a.tree_k + off, kv[i]);
+                            load_bf16<E>(a.tree_v + off, vv[i]);
+                        }
+                    }
+                }
+                float x[4];
+                float mx = m_s;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float dot = 0.f;
+                    if (i < n) {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[i][e], dot);
+                    }
+                    x[i] = warp_sum(dot) * a.scale_log2;
+                    if (i < n) mx = fmaxf(mx, x[i]);
+                }
+                const float al = ptx::ex2(m_s - mx);
+                l_s *= al;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] *= al;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i < n) {
-                        const size_t off =
-                            ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
-                        load_bf16<E>(a.tree_k + off, kv[i]);
-                        load_bf16<E>(a.tree_v + off, vv[i]);
+                        const float p = ptx::ex2(x[i] - mx);
+                        l_s += p;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[i][e], acc[e]);
                     }
                 }
+                m_s = mx;
             }
-            float x[4];
-            float mx = m_s;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float dot = 0.f;
-                if (i < n) {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[i][e], dot);
-                }
-                x[i] = warp_sum(dot) * a.scale_log2;
-                if (i < n) mx = fmaxf(mx, x[i]);
-            }
-            const float al = ptx::ex2(m_s - mx);
-            l_s *= al;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] *= al;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i < n) {
-                    const float p = ptx::ex2(x[i] - mx);
-                    l_s += p;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[i][e], acc[e]);
-                }
-            }
-            m_s = mx;
         }
-    }
 
-    // ---- merge with the partials of the prefix pass
-    ptx::grid_dep_wait();
-    const size_t sf = static_cast<size_t>(slot_floats(D));
-    // Partials are indexed by "virtual slot" v: v < n1 is the folded partial
-    // of prefix CTA c_first + v (copy 0, tile rows r); the rest are those of
-    // c_last: one if it folded, else its F copies (tile rows g * R + r).  This
-    // warp takes v = sub, sub + wpr, ...; its k-th one is v = sub + k * wpr.
-    const int n1 = c_last - c_first;
-    const int nv = (active && nch > 0) ? n1 + (last_folded ? 1 : F) : 0;
-    auto v_cta = [&](int v) -> int { return v < n1 ? c_first + v : c_last; };
-    auto v_copy = [&](int v) -> int { return v < n1 ? 0 : v - n1; };
-    const int nmine = nv > sub ? (nv - sub + wpr - 1) / wpr : 0;
-    // With at least one work-line step per CTA every CTA in [c_first, c_last]
-    // wrote a partial; only when W < C can some of them be empty.
-    const bool every_cta = W >= a.n_ctas;
-    auto v_of = [&](int k) -> int { return sub + k * wpr; };
-    auto v_m = [&](int v) -> size_t {  // offset of m for virtual slot v
-        return static_cast<size_t>(unit + v_cta(v)) * sf + v_copy(v) * R + r;
-    };
-    auto v_acc = [&](int v) -> size_t {  // offset of this lane's accumulator values
-        return static_cast<size_t>(unit + v_cta(v)) * sf + 2 * kRows +
-               static_cast<size_t>(v_copy(v) * R + r) * D + lane * E;
-    };
-    auto v_work = [&](int v) -> bool {
-        return every_cta || cta_has_work(v_cta(v), W, a.n_ctas);
-    };
-    // One round trip: (m, l) of this warp's first 32 partials (lane k: the
-    // k-th) and the accumulator rows of its first four.  Partials are read
-    // through L2 only (ld.global.cg): the prefix grid wrote them while this
-    // grid was resident.
-    // Bit k: the warp's k-th partial exists (one work check per lane, not
-    // one per unrolled load below).
-    const unsigned have = __ballot_sync(kFull, lane < nmine && v_work(v_of(lane)));
-    float m_j = kNegInf, l_j = 0.f;
-    if ((have >> lane) & 1u) {
-        m_j = __ldcg(a.ws + v_m(v_of(lane)));
-        l_j = __ldcg(a.ws + v_m(v_of(lane)) + kRows);
-    }
-    float v[NF][E];
+        // ---- merge with the partials of the prefix pass
+        ptx::grid_dep_wait();
+        const size_t sf = static_cast<size_t>(slot_floats(D));
+        // Partials are indexed by "virtual slot" v: v < n1 is the folded partial
+        // of prefix CTA c_first + v (copy 0, tile rows r); the rest are those of
+        // c_last: one if it folded, else its F copies (tile rows g * R + r).  This
+        // warp takes v = sub, sub + wpr, ...; its k-th one is v = sub + k * wpr.
+        const int n1 = c_last - c_first;
+        const int nv = (active && nch > 0) ? n1 + (last_folded ? 1 : F) : 0;
+        auto v_cta = [&](int v) -> int { return v < n1 ? c_first + v : c_last; };
+        auto v_copy = [&](int v) -> int { return v < n1 ? 0 : v - n1; };
+        const int nmine = nv > sub ? (nv - sub + wpr - 1) / wpr : 0;
+        // With at least one work-line step per CTA every CTA in [c_first, c_last]
+        // wrote a partial; only when W < C can some of them be empty.
+        const bool every_cta = W >= a.n_ctas;
+        auto v_of = [&](int k) -> int { return sub + k * wpr; };
+        auto v_m = [&](int v) -> size_t {  // offset of m for virtual slot v
+            return static_cast<size_t>(unit + v_cta(v)) * sf + v_copy(v) * R + r;
+        };
+        auto v_acc = [&](int v) -> size_t {  // offset of this lane's accumulator values
+            return static_cast<size_t>(unit + v_cta(v)) * sf + 2 * kRows +
+                   static_cast<size_t>(v_copy(v) * R + r) * D + lane * E;
+        };
+        auto v_work = [&](int v) -> bool {
+            return every_cta || cta_has_work(v_cta(v), W, a.n_ctas);
+        };
+        // One round trip: (m, l) of this warp's first 32 partials (lane k: the
+        // k-th) and the accumulator rows of its first four.  Partials are read
+        // through L2 only (ld.global.cg): the prefix grid wrote them while this
+        // grid was resident.
+        // Bit k: the warp's k-th partial exists (one work check per lane, not
+        // one per unrolled load below).
+        const unsigned have = __ballot_sync(kFull, lane < nmine && v_work(v_of(lane)));
+        float m_j = kNegInf, l_j = 0.f;
+        if ((have >> lane) & 1u) {
+            m_j = __ldcg(a.ws + v_m(v_of(lane)));
+            l_j = __ldcg(a.ws + v_m(v_of(lane)) + kRows);
+        }
+        float v[NF][E];
 #pragma unroll
-    for (int j = 0; j < NF; ++j) load_acc<E>(a.ws + v_acc(v_of(j)), (have >> j) & 1u, v[j]);
-    float mx = fmaxf(m_s, m_j);
+        for (int j = 0; j < NF; ++j) load_acc<E>(a.ws + v_acc(v_of(j)), (have >> j) & 1u, v[j]);
+        float mx = fmaxf(m_s, m_j);
 #pragma unroll 1
-    for (int k = 32 + lane; k < nmine; k += 32)  // rare: more than 32 partials per warp
-        if (v_work(v_of(k))) mx = fmaxf(mx, __ldcg(a.ws + v_m(v_of(k))));
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    if (wpr > 1) {
-        if (lane == 0) red_m[warp] = mx;
-        __syncthreads();
-        for (int s2 = 0; s2 < wpr; ++s2) mx = fmaxf(mx, red_m[wr * wpr + s2]);
-    }
-    const bool has_keys = mx != kNegInf;
-    const float w_s = has_keys ? ptx::ex2(m_s - mx) : 0.f;
-    float o[E];
+        for (int k = 32 + lane; k < nmine; k += 32)  // rare: more than 32 partials per warp
+            if (v_work(v_of(k))) mx = fmaxf(mx, __ldcg(a.ws + v_m(v_of(k))));
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        if (wpr > 1) {
+            if (lane == 0) red_m[warp] = mx;
+            __syncthreads();
+            for (int s2 = 0; s2 < wpr; ++s2) mx = fmaxf(mx, red_m[wr * wpr + s2]);
+        }
+        const bool has_keys = mx != kNegInf;
+        const float w_s = has_keys ? ptx::ex2(m_s - mx) : 0.f;
+        float o[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = acc[e] * w_s;
-    float wc = (m_j == kNegInf || !has_keys) ? 0.f : ptx::ex2(m_j - mx);
-    float total = l_s * w_s + warp_sum(wc * l_j);
+        for (int e = 0; e < E; ++e) o[e] = acc[e] * w_s;
+        float wc = (m_j == kNegInf || !has_keys) ? 0.f : ptx::ex2(m_j - mx);
+        float total = l_s * w_s + warp_sum(wc * l_j);
 #pragma unroll
-    for (int j = 0; j < NF; ++j) {
-        const float wj = __shfl_sync(kFull, wc, j);
+        for (int j = 0; j < NF; ++j) {
+            const float wj = __shfl_sync(kFull, wc, j);
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
-    }
-    // Remaining partials of this warp, four accumulator rows per round trip.
+            for (int e = 0; e < E; ++e) o[e] = fmaf(wj, v[j][e], o[e]);
+        }
+        // Remaining partials of this warp, four accumulator rows per round trip.
 #pragma unroll 1
-    for (int k0 = 0; k0 < nmine; k0 += 32) {
-        if (k0 != 0) {
-            const int k = k0 + lane;
-            wc = 0.f;
-            float lc = 0.f;
-            if (k < nmine && v_work(v_of(k))) {
-                const float mm = __ldcg(a.ws + v_m(v_of(k)));
-                wc = (mm == kNegInf) ? 0.f : ptx::ex2(mm - mx);
-                lc = __ldcg(a.ws + v_m(v_of(k)) + kRows);
+        for (int k0 = 0; k0 < nmine; k0 += 32) {
+            if (k0 != 0) {
+                const int k = k0 + lane;
+                wc = 0.f;
+                float lc = 0.f;
+                if (k < nmine && v_work(v_of(k))) {
+                    const float mm = __ldcg(a.ws + v_m(v_of(k)));
+                    wc = (mm == kNegInf) ? 0.f : ptx::ex2(mm - mx);
+                    lc = __ldcg(a.ws + v_m(v_of(k)) + kRows);
+                }
+                total += warp_sum(wc * lc);
             }
-            total += warp_sum(wc * lc);
-        }
-        const int nb = min(32, nmine - k0);
+            const int nb = min(32, nmine - k0);
 #pragma unroll 1
-        for (int j0 = (k0 == 0) ? NF : 0; j0 < nb; j0 += 4) {
-            float wj[4];
+            for (int j0 = (k0 == 0) ? NF : 0; j0 < nb; j0 += 4) {
+                float wj[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                wj[j] = __shfl_sync(kFull, wc, j0 + j);
-                load_acc<E>(a.ws + v_acc(v_of(k0 + j0 + j)), j0 + j < nb && wj[j] != 0.f, v[j]);
+                for (int j = 0; j < 4; ++j) {
+                    wj[j] = __shfl_sync(kFull, wc, j0 + j);
+                    load_acc<E>(a.ws + v_acc(v_of(k0 + j0 + j)), j0 + j < nb && wj[j] != 0.f, v[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[e] = fmaf(wj[j], v[j][e], o[e]);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int e = 0; e < E; ++e) o[e] = fmaf(wj[j], v[j][e], o[e]);
         }
-    }
-    if (wpr > 1) {
-        // Combine the row's warps (all use the same row max mx).
-        if (lane == 0) red_l[warp] = total;
+        if (wpr > 1) {
+            // Combine the row's warps (all use the same row max mx).
+            if (lane == 0) red_l[warp] = total;
 #pragma unroll
-        for (int e = 0; e < E; ++e) red_o[warp][lane * E + e] = o[e];
-        __syncthreads();
-        if (sub != 0) return;
-        for (int s2 = 1; s2 < wpr; ++s2) {
-            total += red_l[warp + s2];
+            for (int e = 0; e < E; ++e) red_o[warp][lane * E + e] = o[e];
+            __syncthreads();
+            if (sub != 0) continue;
+            for (int s2 = 1; s2 < wpr; ++s2) {
+                total += red_l[warp + s2];
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] += red_o[warp + s2][lane * E + e];
+                for (int e = 0; e < E; ++e) o[e] += red_o[warp + s2][lane * E + e];
+            }
         }
-    }
-    if (!active) return;
-    uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
-    float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
-    if (!has_keys) {  // no key at all
+        if (!active) continue;
+        uint16_t* op = a.out + ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * D + lane * E;
+        float* lp = a.lse + (static_cast<size_t>(b) * a.T + t) * a.Hq + h;
+        if (!has_keys) {  // no key at all
 #pragma unroll
-        for (int e = 0; e < E; ++e) op[e] = 0;
-        if (lane == 0) *lp = kNegInf;
-        return;
+            for (int e = 0; e < E; ++e) op[e] = 0;
+            if (lane == 0) *lp = kNegInf;
+            continue;
+        }
+        const float inv = __fdividef(1.f, total);
+        if constexpr (E == 4) {
+            uint2 pk;
+            pk.x = pack_bf16(o[0] * inv, o[1] * inv);
+            pk.y = pack_bf16(o[2] * inv, o[3] * inv);
+            *reinterpret_cast<uint2*>(op) = pk;
+        } else {
+            *reinterpret_cast<uint32_t*>(op) = pack_bf16(o[0] * inv, o[1] * inv);
+        }
+        if (lane == 0) *lp = (mx + log2f(total)) * kLn2;
     }
-    const float inv = __fdividef(1.f, total);
-    if constexpr (E == 4) {
-        uint2 pk;
-        pk.x = pack_bf16(o[0] * inv, o[1] * inv);
-        pk.y = pack_bf16(o[2] * inv, o[3] * inv);
-        *reinterpret_cast<uint2*>(op) = pk;
-    } else {
-        *reinterpret_cast<uint32_t*>(op) = pack_bf16(o[0] * inv, o[1] * inv);
-    }
-    if (lane == 0) *lp = (mx + log2f(total)) * kLn2;
 }
 
 template <typename Kernel, typename... Args>
@@ -1779,16 +1788,20 @@ cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     const long long units = plan.units;
     const int F = plan.F;
     ma.wpr = plan.merge_wpr;
+    ma.rpw = plan.merge_rpw;
     const int rows = M < kRows ? M : kRows;
-    const int rows_per_cta = kMergeWarps / ma.wpr;
+    const int rows_per_cta = kMergeWarps / ma.wpr * ma.rpw;
     const dim3 grid(static_cast<unsigned>(units), (rows + rows_per_cta - 1) / rows_per_cta);
     using K = void (*)(MergeArgs);
-    const K table[2][3] = {
-        {suffix_merge_kernel<D, 1, false>, suffix_merge_kernel<D, 2, false>,
-         suffix_merge_kernel<D, 4, false>},
-        {suffix_merge_kernel<D, 1, true>, suffix_merge_kernel<D, 2, true>,
-         suffix_merge_kernel<D, 4, true>}};
-    const K kernel = table[v.tmode == kTreeNone ? 1 : 0][F == 4 ? 2 : (F == 2 ? 1 : 0)];
+    const K table[3][3] = {
+        {suffix_merge_kernel<D, 1, false, false>, suffix_merge_kernel<D, 2, false, false>,
+         suffix_merge_kernel<D, 4, false, false>},
+        {suffix_merge_kernel<D, 1, false, true>, suffix_merge_kernel<D, 2, false, true>,
+         suffix_merge_kernel<D, 4, false, true>},
+        {suffix_merge_kernel<D, 1, true, false>, suffix_merge_kernel<D, 2, true, false>,
+         suffix_merge_kernel<D, 4, true, false>}};
+    const int form = v.tmode == kTreeNone ? 2 : (ma.rpw > 1 ? 1 : 0);
+    const K kernel = table[form][F == 4 ? 2 : (F == 2 ? 1 : 0)];
     return launch_pdl(kernel, grid, dim3(32 * kMergeWarps), 0, stream, ma);
 }
 

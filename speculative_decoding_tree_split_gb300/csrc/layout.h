@@ -299,10 +299,15 @@ TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>
 //              for the unfolded copies of the last CTA.
 struct Plan {
     int G, M, RB, units, F, n_ctas, merge_wpr;
+    int merge_rpw;  // merge rows per warp, taken in turn
     int tmode;  // TreeMode chosen for the call
     int ovh;    // overhead slots per unit on the work line (unit_len)
     long long max_steps;
 };
+
+// Merge kernel: warps per CTA, and CTAs its register budget lets an SM hold.
+constexpr int kMergeWarps = 4;
+constexpr int kMergeResident = 6;
 
 // Overhead slots per unit: a segment switch costs about as much as 2 + F*M/24
 // 64-key steps (measured: the epilogue stores F*M rows of partials, then the
@@ -362,6 +367,19 @@ TA_HD Plan make_plan(int B, int Hq, int Hkv, int T, int P, int max_pages, int sm
     // sees about one partial per CTA plus the F copies of a straddling CTA.
     const long long expect = p.n_ctas / units + 1 + p.F;
     p.merge_wpr = expect > 12 ? 4 : (expect > 6 ? 2 : 1);
+    // Without a tree pass a merge warp's rows are cheap: give each warp
+    // several, in turn, rather than launch more CTAs than the SMs hold at
+    // once (kMergeResident per SM), whose later waves would wait for the
+    // earlier ones.
+    p.merge_rpw = 1;
+    if (p.tmode != kTreeNone) {
+        const long long rows = p.M < kRows ? p.M : kRows;
+        const long long per_cta = kMergeWarps / p.merge_wpr;
+        const long long ctas = units * ((rows + per_cta - 1) / per_cta);
+        const long long cap = static_cast<long long>(sm_count) * kMergeResident;
+        p.merge_rpw = static_cast<int>(cap > 0 ? (ctas + cap - 1) / cap : 1);
+        if (p.merge_rpw < 1) p.merge_rpw = 1;
+    }
     return p;
 }
 

@@ -194,6 +194,7 @@ int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_size, int max_
     out->replicas = p.F;
     out->n_ctas = p.n_ctas;
     out->merge_warps_per_row = p.merge_wpr;
+    out->merge_rows_per_warp = p.merge_rpw;
     out->max_steps = p.max_steps;
     out->workspace_bytes = ws_bytes(B, Hq, Hkv, d, T, p.n_ctas);
     return TREE_ATTN_OK;

@@ -321,6 +321,24 @@ def test_full_size_verify_tree(oracle, name):
     assert np.abs(got_l - ref_l).max() <= LSE_TOL
 
 
+def test_merge_rows_per_warp(oracle):
+    # 16 x 8 units x 64 rows with the tree on the prefix pass (a small call):
+    # 2048 single-row merge CTAs would not fit at once, so each merge warp
+    # takes several rows in turn; every row against the oracle, both APIs.
+    cfg = Config("rpw", B=16, Hq=64, Hkv=8, d=128, L=(0, 300), page=16, T=8, max_depth=3,
+                 max_branch=3, seed=96)
+    wl = make_workload(cfg)
+    p = ta.plan(16, 64, 8, 128, 8, 16, wl.max_pages_per_seq)
+    assert p["tree_in_prefix"] == 1 and p["merge_rows_per_warp"] > 1
+    out, lse = compare_all(oracle, wl)
+    x = to_dev(wl)
+    o2, l2 = ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["seq_lens"],
+                            x["tree_k"], x["tree_v"], x["parents"], softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(o2.float().cpu().numpy(), out)
+    assert np.array_equal(l2.cpu().numpy(), lse)
+
+
 @pytest.mark.parametrize("T,G,n_ctas", [(4, 4, 2), (8, 4, 3), (12, 4, 2), (16, 4, 2), (20, 4, 1),
                                         (16, 5, 2)])
 def test_row_replication_paths(oracle, T, G, n_ctas):

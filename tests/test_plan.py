@@ -55,10 +55,17 @@ def test_plan_llama8b_and_tiny_by_hand():
 
 
 def test_plan_other_workloads_by_hand():
-    # llama70b: M = 8 * 8 = 64 -> 2 replicas; units 16*8 = 128; 152 // 128 = 1 -> 1+1+2 = 4
+    # llama70b: M = 8 * 8 = 64 -> 2 replicas; units 16*8 = 128; 152 // 128 = 1 -> 1+1+2 = 4;
+    # tree on the prefix pass, merge alone: 128 units x 64/4 CTAs = 2048 > 152 x 6 = 912 CTAs
+    # at once -> ceil(2048 / 912) = 3 rows per merge warp
     c = CONFIGS["llama70b"]
     p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
     assert (p["units"], p["replicas"], p["n_ctas"], p["merge_warps_per_row"]) == (128, 2, 152, 1)
+    assert p["merge_rows_per_warp"] == 3
+    for name in ("tiny", "llama8b", "chain", "maverick"):
+        c = CONFIGS[name]
+        p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
+        assert p["merge_rows_per_warp"] == 1, name
     # chain: M = 4 * 4 = 16 -> 4 replicas; units 512; 0 + 1 + 4 = 5 -> 1 warp
     c = CONFIGS["chain"]
     p = ta.plan(c.B, c.Hq, c.Hkv, c.d, c.T, c.page, max_pages(c), SMS)
@@ -86,6 +93,13 @@ def test_plan_invariants(B, Hq, Hkv, d, T, P, maxp):
     want_tree = prefix_steps <= 32 * C or (p["units"] <= C and p["replicas"] >= 2)
     assert p["tree_in_prefix"] == int(want_tree)
     assert p["max_steps"] == prefix_steps + (p["units"] if want_tree else 0)
+    # the merge alone (tree on the prefix pass) gives each warp several rows
+    # when one row per warp would need more CTAs than 6 per SM
+    rows = min(M, 128)
+    per_cta = 4 // p["merge_warps_per_row"]
+    ctas = p["units"] * -(-rows // per_cta)
+    want_rpw = max(1, -(-ctas // (SMS * 6))) if want_tree else 1
+    assert p["merge_rows_per_warp"] == want_rpw
     assert 1 <= p["n_ctas"] <= min(SMS, max(1, p["max_steps"]))
     if p["row_blocks"] == 1:
         assert p["replicas"] * M <= 128 or p["replicas"] == 1
