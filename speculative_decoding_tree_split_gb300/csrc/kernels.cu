@@ -286,125 +286,10 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     }
 }
 
-// Committed-prefix steps whose K/V one CTA pulls into L2 before it waits for
-// the previous kernel (8 steps = 4 blocks = 256 KB for d = 128).
-constexpr int kSpecSteps = 8;
-
-// Runs before the kernel waits for its predecessor (programmatic dependent
-// launch): pull the first K/V tiles of this CTA's range into L2, so that the
-// producer's first loads after the wait hit L2 instead of HBM.  This is a
-// guess and only a hint.  seq_lens and block_table may still be being written
-// by the predecessor, so they are read through L2 only (ld.global.cg: never
-// cached in L1, where a stale line could outlive the wait), every index that
-// comes out of them is clamped into range, and all that is issued is L2
-// prefetches, which cannot change any result (L2 is where the predecessor's
-// writes land).  The CTA's real plan is made after the wait from fresh reads.
-// One warp, all lanes; lane i takes work-line step i of the range.
-template <int D>
-__device__ void speculative_l2_prefetch(const PrefixArgs& a, int lane, const CUtensorMap* tm_k,
-                                        const CUtensorMap* tm_v) {
-    if (a.B > 32 * kPlanRegs) return;  // one round trip for the lengths, or nothing
-    const int upb = a.Hkv * a.RB;
-    int32_t lraw[kPlanRegs];
-#pragma unroll
-    for (int i = 0; i < kPlanRegs; ++i) {
-        const int b = 32 * i + lane;
-        lraw[i] = b < a.B ? __ldcg(a.seq_lens + b) : 0;
-    }
-    int nreg[kPlanRegs];
-    long long tot = 0;
-#pragma unroll
-    for (int i = 0; i < kPlanRegs; ++i) {
-        bool bad;
-        nreg[i] = 32 * i + lane < a.B
-                      ? unit_len(unit_chunks(lraw[i], a.P, a.max_pages, a.tmode, a.T, bad), a.ovh)
-                      : 0;
-        if (32 * i < a.B) tot += __reduce_add_sync(kFull, nreg[i]);
-    }
-    const long long W = tot * upb;
-    if (W <= 0) return;
-    const long long x0 = cta_start(blockIdx.x, W, a.n_ctas);
-    const long long x1 = cta_start(blockIdx.x + 1, W, a.n_ctas);
-    if (x0 >= x1) return;
-    // Sequence holding x0 and the work-line position of its first unit.
-    int b0 = -1;
-    long long base0 = 0, run = 0;
-#pragma unroll
-    for (int i = 0; i < kPlanRegs; ++i) {
-        if (b0 >= 0 || 32 * i >= a.B) continue;
-        const long long n = static_cast<long long>(upb) * nreg[i];
-        const long long incl = warp_incl_scan(n, lane);
-        const long long excl = incl - n;
-        const unsigned m =
-            __ballot_sync(kFull, 32 * i + lane < a.B && run + excl <= x0 && x0 < run + incl);
-        if (m != 0) {
-            const int src = __ffs(m) - 1;
-            b0 = 32 * i + src;
-            base0 = run + __shfl_sync(kFull, excl, src);
-        }
-        run += __shfl_sync(kFull, incl, 31);
-    }
-    if (b0 < 0) return;
-    int32_t L_raw = 0;
-#pragma unroll
-    for (int i = 0; i < kPlanRegs; ++i) {
-        const int32_t v = __shfl_sync(kFull, lraw[i], b0 & 31);
-        if (b0 / 32 == i) L_raw = v;
-    }
-    bool bad;
-    const int L = clamp_seq_len(L_raw, a.P, a.max_pages, bad);
-    const int nch = unit_chunks(L_raw, a.P, a.max_pages, a.tmode, a.T, bad);
-    const int len = unit_len(nch, a.ovh);
-    if (len <= 0) return;
-    const long long off = x0 - base0;
-    const int urel = static_cast<int>(div_nn(off, len));
-    const int pos = static_cast<int>(off - static_cast<long long>(urel) * len);
-    if (urel >= upb) return;
-    const int hk = min(urel / a.RB, a.Hkv - 1);
-    // Step `lane` of the range, if it is a committed-prefix step.
-    const long long steps = min(static_cast<long long>(nch - pos), x1 - x0);
-    const int ch = pos + lane;
-    if (lane >= kSpecSteps || lane >= steps || static_cast<long long>(ch) * kChunk >= L) return;
-    const int Pb = a.P < kChunk ? a.P : kChunk;
-    const int32_t* bt = a.block_table + static_cast<size_t>(b0) * a.max_pages;
-    int pids[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int tok = ch * kChunk + i * Pb;
-        const int lp = tok / a.P;
-        pids[i] = (i * Pb < kChunk && tok < L && lp < a.max_pages) ? __ldcg(bt + lp) : -1;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int tok = ch * kChunk + i * Pb;
-        if (pids[i] < 0) continue;
-        const int pid = min(pids[i], a.num_pages - 1);
-        const int y = (pid * a.Hkv + hk) * a.P + tok % a.P;
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-            ptx::tma_prefetch_2d(tm_k, h * 64, y);
-            ptx::tma_prefetch_2d(tm_v, h * 64, y);
-        }
-    }
-}
-
 // Barrier among `count` threads (whole warps) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-
-// Arrive at hardware barrier `id` without waiting (memory operations before it
-// are visible to the threads that complete the barrier with bar.sync).
-__device__ __forceinline__ void named_bar_arrive(int id, int count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Hardware barrier ids (0 is __syncthreads): the epilogue's fold among the
-// softmax warps; the set-up hand-over (barriers, TMEM) to warps 0-4; the
-// plan hand-over from warp 0 to the MMA warp.
-constexpr int kBarFold = 1;
-constexpr int kBarSetup = 2;
-constexpr int kBarPlan = 3;
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -465,27 +350,15 @@ __global__ void __launch_bounds__(192, 1)
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
     }
-    // L2 policy of the K/V loads (reads no input, so it is made before the wait).
-    const uint64_t pol = (warp == 4 && lane == 0) ? ptx::policy_evict_first() : 0ull;
     if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), S::TMEM_COLS);
         ptx::tmem_relinquish();
-        ptx::tc_fence_before();
-        named_bar_arrive(kBarSetup, 192);  // the TMEM address, to warps 0-4
-        // The MMA warp has nothing to do until the first K/V lands: it guesses
-        // the CTA's first tiles and pulls them into L2 while the previous
-        // kernel finishes.
-        if constexpr (!DENSE) speculative_l2_prefetch<D>(a, lane, &tm_k, &tm_v);
-        __syncwarp();
-        ptx::grid_dep_wait();
-        named_bar_sync(kBarPlan, 64);  // warp 0 has published the plan
-        ptx::tc_fence_after();
     }
-    if (warp != 5) {
-        // Inputs may come from the kernel before us in the stream.
-        ptx::grid_dep_wait();
-        if (warp == 0) compute_plan(a, lane, misc);
-    }
+    // L2 policy of the K/V loads (reads no input, so it is made before the wait).
+    const uint64_t pol = (warp == 4 && lane == 0) ? ptx::policy_evict_first() : 0ull;
+    // Inputs may come from the kernel before us in the stream.
+    ptx::grid_dep_wait();
+    if (warp == 0) compute_plan(a, lane, misc);
     if (warp == 4) {
         // A small block table is pulled into L1 while the plan is computed, so
         // the producer's first page lookups do not each wait for L2.
@@ -497,12 +370,9 @@ __global__ void __launch_bounds__(192, 1)
             if (lane + 32 < lines) ptx::prefetch_l1(bt + static_cast<size_t>(lane + 32) * kL1Line);
         }
     }
-    if (warp != 5) {
-        ptx::tc_fence_before();
-        named_bar_sync(kBarSetup, 192);  // warps 0-4 wait; warp 5 arrived above
-        ptx::tc_fence_after();
-        if (warp == 0) named_bar_arrive(kBarPlan, 64);
-    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
     ptx::grid_dep_launch();
     const uint32_t tmem = misc->tmem_base;
     const int upb = a.Hkv * a.RB;
@@ -1108,7 +978,7 @@ __global__ void __launch_bounds__(192, 1)
                         stg_ml[(g * R + lr) * 2 + 1] = l_sum;
                     }
                 }
-                named_bar_sync(kBarFold, 128);
+                named_bar_sync(1, 128);
                 // RU rows per warp at a time: their shared-memory reads are
                 // all issued before any is used.
                 constexpr int RU = 4 / F;

@@ -89,15 +89,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// Prefetch a 2-D tile of the tensor into L2 (no shared memory, no barrier;
-// a hint only: nothing waits for it and a later load of the tile hits L2).
-__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // 3-D tiled tensor load into shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                             int32_t z, uint32_t bar, uint64_t policy) {
