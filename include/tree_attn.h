@@ -361,8 +361,9 @@ typedef struct tree_attn_plan_info {
                              /* (+1 per unit when the tree rides on the prefix pass) */
     size_t workspace_bytes;  /* partial-result slots for this n_ctas                 */
     int tree_in_prefix;      /* 1: the prefix pass attends the tree tokens too (one   */
-                             /* masked chunk per unit; small, latency-bound calls);   */
-                             /* 0: the suffix/merge kernel attends them               */
+                             /* masked chunk per unit: calls of at most 32 steps per  */
+                             /* CTA, or with no more units than CTAs and 2 or more    */
+                             /* row copies); 0: the suffix/merge kernel attends them  */
     int merge_rows_per_warp; /* query rows each merge warp takes in turn (> 1 only    */
                              /* when the tree is on the prefix pass and one row per   */
                              /* warp would need more merge CTAs than the SMs hold)    */

@@ -292,11 +292,14 @@ TA_HD long long slot_floats(int d) { return 2LL * kRows + static_cast<long long>
 //              would otherwise launch CTAs with nothing to do);
 //   F          query-row copies per tile when one 128-row block holds the
 //              unit's rows (small M: the softmax work per CTA is split);
-//   tmode      whether the tree tokens ride on the prefix pass (small,
-//              latency-bound calls) or are attended by the merge kernel;
+//   tmode      whether the tree tokens ride on the prefix pass (small calls,
+//              and calls with no more units than CTAs and two or more row
+//              copies) or are attended by the merge kernel;
 //   merge_wpr  warps per query row in the merge, from the partials a row
 //              expects: prefix CTAs per unit, +1 for a straddled end, +F
-//              for the unfolded copies of the last CTA.
+//              for the unfolded copies of the last CTA;
+//   merge_rpw  rows each merge warp takes in turn (merge without the tree
+//              pass, when one row per warp would not fit the SMs at once).
 struct Plan {
     int G, M, RB, units, F, n_ctas, merge_wpr;
     int merge_rpw;  // merge rows per warp, taken in turn

@@ -335,7 +335,7 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
     // The tree tokens ride on the prefix pass's work line: one extra chunk
     // per unit from the tree buffers, or the positions after the prefix when
     // they are padded into the cache.  The explicit-mask form has no tree.
-    // The kernel selector decides which (small calls: on the line).
+    // The kernel selector decides which (see make_plan).
     Plan plan;
     if (!plan_call(n_ctas, B, Hq, Hkv, T, page_size, max_pages_per_seq,
                    dense != nullptr ? kTreeNone : (tree_in_cache ? kTreeInCache : kTreeChunk),
