@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 # source whose SHA-256 is recorded with it (see profiles/).
 NCU_TRAFFIC = {
     # Llama-3.1-8B layer, mean of three launches of one ncu capture
-    "llama8b": ("9554d00bf18dc3bd", 33736874),
+    "llama8b": ("402ec8fece82c130", 33736874),
 }
 
 
@@ -102,13 +102,19 @@ def measured_hbm_peak():
 
 
 def kernel_source_sha():
-    """SHA-256 prefix of the device sources the prefix-pass kernel is built from."""
+    """SHA-256 prefix of the device sources the prefix-pass kernel is built from,
+    with comments and whitespace removed (a comment edit does not make a traffic
+    record stale; any code change does)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in ("kernels.cu", "layout.h", "ptx.cuh"):
         with open(os.path.join(_ROOT, "speculative_decoding_tree_split_gb300", "csrc", name),
-                  "rb") as f:
-            h.update(f.read())
+                  encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
