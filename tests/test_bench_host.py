@@ -71,3 +71,31 @@ def test_reference_arm_other_ranks_print_nothing():
                         "--config", "tiny", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_kernel_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    # The ncu traffic record is keyed by this hash: a comment or whitespace
+    # edit must keep it, any code edit must change it.
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "speculative_decoding_tree_split_gb300", "csrc")
+    dst = tmp_path / "speculative_decoding_tree_split_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    texts = {}
+    for name in ("kernels.cu", "layout.h", "ptx.cuh"):
+        with open(os.path.join(src, name), encoding="utf-8") as f:
+            texts[name] = f.read()
+
+    def sha_with(layout_text):
+        for name, text in texts.items():
+            (dst / name).write_text(layout_text if name == "layout.h" else text, encoding="utf-8")
+        monkeypatch.setattr(bench, "_ROOT", str(tmp_path))
+        return bench.kernel_source_sha()
+
+    base = sha_with(texts["layout.h"])
+    commented = texts["layout.h"] + "\n// a new comment\n/* and a\n   block comment */\n\n   \n"
+    assert sha_with(commented) == base
+    code = texts["layout.h"].replace("constexpr int kTreeInPrefixMaxSteps = 32;",
+                                     "constexpr int kTreeInPrefixMaxSteps = 33;")
+    assert code != texts["layout.h"]
+    assert sha_with(code) != base
