@@ -528,7 +528,8 @@ __global__ void __launch_bounds__(192, 1)
                     if (np < nq) {
                         const uint32_t j = jj + np;
                         if (ptx::mbar_try_wait(bar(S::P_FULL + (j & 1)), (j >> 1) & 1) &&
-                            (np > 0 || kk == 0 || ptx::mbar_try_wait(bar(S::O_FREE), (kk - 1) & 1))) {
+                            (np > 0 || kk == 0 ||
+                             ptx::mbar_try_wait(bar(S::O_FREE), (kk - 1) & 1))) {
                             ptx::tc_fence_after();
                             const uint32_t vst =
                                 sb + S::OFF_STAGE + (j % S::NS) * S::STAGE_BYTES + S::TILE_BYTES;
@@ -558,14 +559,16 @@ __global__ void __launch_bounds__(192, 1)
                         const uint32_t j = jj + nq;
                         const int s = j % S::NS;
                         if (ptx::mbar_try_wait(bar(S::KV_FULL + s), (j / S::NS) & 1) &&
-                            (j < 2 || ptx::mbar_try_wait(bar(S::S_FREE + (j & 1)), ((j >> 1) - 1) & 1))) {
+                            (j < 2 ||
+                             ptx::mbar_try_wait(bar(S::S_FREE + (j & 1)), ((j >> 1) - 1) & 1))) {
                             ptx::tc_fence_after();
                             const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
                             const uint32_t d_s = tmem + S::TM_S + (j & 1) * kBlock;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
                                 const uint64_t ad = smem_desc_sw128(
-                                    sb + S::OFF_Q + (k >> 2) * S::QATOM_BYTES + (k & 3) * 32, 16, 1024);
+                                    sb + S::OFF_Q + (k >> 2) * S::QATOM_BYTES + (k & 3) * 32, 16,
+                                    1024);
                                 const uint64_t bd = smem_desc_sw128(
                                     kst + (k >> 2) * S::HALF_BYTES + (k & 3) * 32, 16, 1024);
                                 ptx::mma_bf16(d_s, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
@@ -707,7 +710,8 @@ __global__ void __launch_bounds__(192, 1)
             auto chunk_vis = [&](int c) -> uint64_t {
                 if (c >= cur.chunk_end) return 0ull;
                 if (TM == kTreeChunk && c == tree_ch) return tbits;
-                const long long rem = static_cast<long long>(L) - static_cast<long long>(c) * kChunk;
+                const long long rem =
+                    static_cast<long long>(L) - static_cast<long long>(c) * kChunk;
                 uint64_t v = rem >= kChunk ? ~0ull : (rem <= 0 ? 0ull : ((1ull << rem) - 1ull));
                 if (TM == kTreeInCache) {
                     if (rem >= 0)
@@ -865,7 +869,8 @@ __global__ void __launch_bounds__(192, 1)
                             sp[i & 7] += s[i];
                         }
                     }
-                    l_sum += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+                    l_sum += ((sp[0] + sp[1]) + (sp[2] + sp[3])) +
+                             ((sp[4] + sp[5]) + (sp[6] + sp[7]));
                 }
                 // P buffer (jj & 1) is free once PV(jj - 2) has completed.
                 if (jj >= 2 && !wait_all(bar(S::P_FREE + (jj & 1)), ((jj >> 1) - 1) & 1)) {
@@ -1310,7 +1315,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int i = lane + 32 * hh;
-                    if (i < a.T) a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
+                    if (i < a.T)
+                        a.mask_out[static_cast<size_t>(b) * a.parents_stride + i] = anc[hh];
                 }
             }
         } else if (suffix_here && a.mask != nullptr && active && sub == 0) {
@@ -1346,7 +1352,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
                         page[i] = -1;
                         const int pos = L_b + js[i];
                         if (i < n && pos / a.P < a.max_pages)
-                            page[i] = a.block_table[static_cast<size_t>(b) * a.max_pages + pos / a.P];
+                            page[i] =
+                                a.block_table[static_cast<size_t>(b) * a.max_pages + pos / a.P];
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -1354,8 +1361,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
                         const int pos = L_b + js[i];
                         if (page[i] < 0 || page[i] >= a.num_pages) {
                             if (lane == 0)
-                                report(a.status, pos / a.P < a.max_pages ? TREE_ATTN_STATUS_BAD_PAGE
-                                                                         : TREE_ATTN_STATUS_BAD_SEQ_LEN);
+                                report(a.status, pos / a.P < a.max_pages
+                                                     ? TREE_ATTN_STATUS_BAD_PAGE
+                                                     : TREE_ATTN_STATUS_BAD_SEQ_LEN);
 #pragma unroll
                             for (int e = 0; e < E; ++e) kv[i][e] = vv[i][e] = 0.f;
                             continue;
@@ -1371,7 +1379,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
                     for (int i = 0; i < 4; ++i) {
                         if (i < n) {
                             const size_t off =
-                                ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D + lane * E;
+                                ((static_cast<size_t>(b) * a.T + js[i]) * a.Hkv + hk) * D +
+                                lane * E;
                             load_bf16<E>(a.tree_k + off, kv[i]);
                             load_bf16<E>(a.tree_v + off, vv[i]);
                         }
