@@ -221,14 +221,16 @@ def emit(obj):
 # ---------------------------------------------------------------------------
 # CPU side: the fp64 oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_token_fn(wl, layout="shared"):
+def oracle_token_fn(wl, layout="shared", threads=None):
     """f(b, i): the oracle on one tree token (all Hq query heads of sequence b,
     node i), with sequence b's own tree mask (the one-pass oracle under the
-    explicit mask for the full_mask layout)."""
+    explicit mask for the full_mask layout).  threads: the oracle's OpenMP
+    threads (default: every core this process may run on)."""
     import oracle
     orc = oracle.get()
     c = wl.cfg
-    threads = len(os.sched_getaffinity(0))
+    if threads is None:
+        threads = len(os.sched_getaffinity(0))
     if layout == "full_mask":
         from oracle.dense import dense_mask
         tm = orc.tree_mask(wl.parents.tolist())
@@ -257,11 +259,11 @@ def oracle_token_fn(wl, layout="shared"):
     return f, threads
 
 
-def oracle_tokens_per_s(wl, budget_s, max_tokens=None, layout="shared"):
+def oracle_tokens_per_s(wl, budget_s, max_tokens=None, layout="shared", threads=None):
     """Time the oracle on whole tree tokens (all Hq heads of one (b, i)),
     round-robin over the batch, until `budget_s` of wall time is spent."""
     c = wl.cfg
-    f, threads = oracle_token_fn(wl, layout)
+    f, threads = oracle_token_fn(wl, layout, threads)
     tokens = [(b, i) for b in range(c.B) for i in range(c.T)]
     done = 0
     t0 = time.perf_counter()
@@ -493,9 +495,13 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, n_tok, el, threads = oracle_tokens_per_s(wl, args.cpu_seconds, layout=layout)
+        # the same on one core, for a third of the time
+        v1, n1, el1, _ = oracle_tokens_per_s(wl, args.cpu_seconds / 3, layout=layout, threads=1)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n_tok} tree tokens (all {cfg.Hq} query heads each) of this "
-                         f"workload, round-robin, {el:.1f} s of fp64 oracle time"}
+                         f"workload, round-robin, {el:.1f} s of fp64 oracle time",
+               "value_1_core": v1,
+               "sample_1_core": f"{n1} tree tokens, {el1:.1f} s, one thread"}
 
     if rank == 0:
         emit({
