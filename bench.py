@@ -422,6 +422,11 @@ def run_ours(args):
         barrier()
         return s.elapsed_time(e)
 
+    # Each graph's first launch uploads it to the device: launch the timed
+    # graphs once, untimed, so that the timed replays hold only the steps.
+    g_timed.replay()
+    g_prefix.replay()
+    torch.cuda.synchronize()
     # warm-up replays (W steps), then keep the GPU loaded ~1 s so the clock
     # sampler sees the timed region's clocks, then the timed K steps.
     g_warm.replay()
@@ -441,6 +446,11 @@ def run_ours(args):
     ms_step = ms_total / K
     ms_prefix = ms_prefix_total / K
     ms_step, ms_prefix = max_over_ranks([ms_step, ms_prefix], dev)
+    # Run-to-run spread: the same K-step graph replayed five more times, each
+    # timed alone.  Reported beside `value`, which is the one timed region above.
+    reps = sorted(max_over_ranks([timed(g_timed) / K for _ in range(5)], dev))
+    spread = {"replays": len(reps), "us_per_step_min": reps[0] * 1e3,
+              "us_per_step_median": reps[len(reps) // 2] * 1e3, "us_per_step_max": reps[-1] * 1e3}
     tokens_per_step = cfg.B * cfg.T * world
     value = tokens_per_step / (ms_step * 1e-3)
 
@@ -524,7 +534,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": nbytes["prefix_kernel"],
                          "peak_source": peak_src, "kernel_sha": sha},
             "clocks": clocks, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP[layout] * K,
-            "cpu_baseline": cpu,
+            "cpu_baseline": cpu, "spread": spread,
         })
     if world > 1:
         import torch.distributed as dist
@@ -651,7 +661,10 @@ def run_accept_commit(args):
         return s_.elapsed_time(e_) / K
 
     g_step, g_acc, g_com = graph_of(step), graph_of(accept_only), graph_of(commit_only)
+    # first launches upload the graphs; keep that out of the timed replays
     g_step.replay()
+    g_acc.replay()
+    g_com.replay()
     sampler = ClockSampler(smi_gpu_id(torch.cuda.get_device_properties(dev), local))
     if not args.no_clocks:
         sampler.start()
