@@ -10,8 +10,9 @@
  * themselves under the tree mask -- and the two partial results are merged by
  * log-sum-exp ("merge_attentions", the combination of attention over disjoint
  * KV chunks named in the review's supporting citations).  The prefix lives in
- * a paged KV cache ("paged/persistent KV-cache handling for tree attention",
- * review, Referee Report summary) and is processed split over its length in
+ * a paged KV cache (the review's Referee Report summary counts paged,
+ * persistent KV handling among what tree attention needs) and is processed
+ * split over its length in
  * the manner of flash-decoding (Dao, Haziza, Massa, Sizov, cited in the
  * review's reference list).
  *
@@ -215,7 +216,7 @@ TREE_ATTN_API int tree_attn_verify_tree(const uint16_t *q, const uint16_t *k_pag
 
 /*
  * tree_attn_verify_paged_tree -- split tree attention with the draft tokens
- * padded into the paged KV cache ("paged KV with tree padding", pith.science
+ * padded into the paged KV cache (the padded layout named in the pith.science
  * verdict record, desk editor's note): tree token j of sequence b has its
  * K/V at logical position seq_lens[b] + j of that sequence's pages, so the
  * block table must cover seq_lens[b] + T tokens (else status
@@ -252,8 +253,8 @@ TREE_ATTN_API int tree_accept_commit(const uint64_t *mask, int mask_stride,
 
 /*
  * tree_dense_mask_build / tree_attn_verify_dense -- the one-pass form of tree
- * attention under an explicit mask: the "giant explicit mask" that split tree
- * attention replaces (pith.science review of arXiv 2508.08192, "What carries
+ * attention under an explicit mask: the very large explicit mask that split
+ * tree attention replaces (pith.science review of arXiv 2508.08192, "What carries
  * the argument").  Kept as an ablation of the split form; both compute the
  * same attention.  The tree tokens must sit in the paged cache after each
  * prefix (tree_attn_verify_paged_tree layout).
@@ -376,8 +377,8 @@ TREE_ATTN_API int tree_attn_plan(int B, int Hq, int Hkv, int d, int T, int page_
 /*
  * tree_attn_prefix_pass / tree_attn_suffix_merge -- the two passes of
  * tree_attn_verify as separate calls (tree_attn_verify_ctas == prefix pass
- * then suffix merge, same arguments).  The prefix pass ("attention from query
- * to the prefix context ... no custom mask needed", pith.science review,
+ * then suffix merge, same arguments).  The prefix pass (the tree tokens
+ * against the committed prefix, which needs no mask: pith.science review,
  * "What carries the argument") writes one partial result (running max m,
  * sum l, unnormalised accumulator acc, base-2 exponent domain) per split of
  * the prefix into `workspace`.  The suffix merge computes the tree part under

@@ -2,9 +2,9 @@
 (oracle; importable by the tests, the smoke check and the benchmark's CPU
 legs only).
 
-"Giant explicit mask" is the form split tree attention avoids (pith.science
-review of arXiv 2508.08192, "What carries the argument"); with the tree
-tokens padded into the paged cache ("paged KV with tree padding",
+One explicit mask over every key is the form split tree attention avoids
+(pith.science review of arXiv 2508.08192, "What carries the argument"); with
+the tree tokens padded into the paged cache (the padded layout of the
 pith.science verdict record, desk editor's note) the mask of tree token i of
 sequence b over cache position p is written out below.  Pinned through
 ``oracle_dense_rows`` equalling the split definition (tests/oracle_pins.py);

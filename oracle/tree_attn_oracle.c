@@ -278,11 +278,11 @@ int oracle_chunk_rows(const uint16_t *q, const uint16_t *k_pages, const uint16_t
 /*
  * Tree attention in one pass with an explicit mask: the "naive" form that
  * split tree attention replaces (pith.science review of 2508.08192, "What
- * carries the argument": instead of one attention under a giant explicit mask,
- * the prefix and the tree are attended separately and merged).
+ * carries the argument": rather than one attention under a very large
+ * explicit mask, the prefix and the tree are attended separately and merged).
  *
  * Every key sits in the paged cache -- the tree tokens too, at positions
- * L_b .. L_b + T - 1 ("paged KV with tree padding", pith.science verdict
+ * L_b .. L_b + T - 1 (the padded layout of the pith.science verdict
  * record, desk editor's note) -- and query row (b, i, h) attends key
  * position p in [0, key_lens[b]) exactly when dense[(b * T + i) * cols + p]
  * is non-zero.  Same score, log-sum-exp and value sum as attend_chunk,

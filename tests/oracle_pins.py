@@ -12,8 +12,8 @@ Facts used (none of them is the oracle's own formula retyped):
   pith.science review of 2508.08192, "What carries the argument").  Checked
   by enumerating root-to-node paths with a depth-first walk over child lists,
   for every valid parent array up to T = 7.
-* Attention: a dense explicit-mask attention (the "giant explicit mask" form
-  the same section contrasts split attention with) evaluated by
+* Attention: a dense explicit-mask attention (the one-mask-over-every-key
+  form the same section contrasts split attention with) evaluated by
   ``torch.nn.functional.scaled_dot_product_attention`` in float64 over K/V
   gathered into contiguous arrays; its LSE by ``torch.logsumexp``.
 * Closed forms: q = 0 gives lse = ln(number of attended keys) and out = the

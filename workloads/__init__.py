@@ -8,8 +8,9 @@ here, so that the two sides see the same bits.
 Workload shapes follow the Llama-shaped verification layers that the review
 pages of "Efficient Speculative Decoding for Llama at Scale: Challenges and
 Solutions" (arXiv 2508.08192) describe: an EAGLE draft tree of ``T`` tokens
-verified against a paged KV cache ("paged/persistent KV-cache handling for tree
-attention", pith.science review, Referee Report summary). The pages print no
+verified against a paged KV cache (the pith.science review's Referee Report
+summary counts paged, persistent KV handling among what tree attention needs).
+The pages print no
 tensor shapes; the five shapes below are the stated synthetic stand-ins.
 
 Recipe (all draws come from one ``torch.Generator('cpu')`` seeded per config):
@@ -31,8 +32,8 @@ Two layout variants (both off by default, so the default draws are unchanged):
 
 * ``per_sequence_trees``: step 2 runs once per sequence, giving ``parents``
   of shape [B][T] (one draft tree per sequence).
-* ``tree_in_cache``: the tree tokens live in the paged cache ("paged KV with
-  tree padding"): each sequence's pages cover ``L_b + T`` positions and token
+* ``tree_in_cache``: the tree tokens live in the paged cache, padded after
+  the prefix: each sequence's pages cover ``L_b + T`` positions and token
   ``j``'s K/V (the same ``tree_k`` / ``tree_v`` draws) is written at logical
   position ``L_b + j``.
 """
