@@ -821,6 +821,10 @@ __global__ void __launch_bounds__(192, 1)
                         if (((w >> (8 * (i % 4))) & 0xffu) == 0) s[i] = kNegInf;
                     }
                 }
+                // Blocks whose rounding of P to bf16 is tracked (see the epilogue).
+                const bool track = DENSE || (TM != kTreeNone && !plain &&
+                                             ((TM == kTreeChunk && ch + nh > tree_ch) ||
+                                              (TM == kTreeInCache && (ch + nh) * kChunk > L)));
                 if (row_ok) {
                     // Eight independent partial maxima / sums keep the
                     // dependency chains short.
@@ -847,27 +851,10 @@ __global__ void __launch_bounds__(192, 1)
                     float sp[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) sp[u] = 0.f;
-                    const bool track = DENSE || (TM != kTreeNone && !plain &&
-                                                 ((TM == kTreeChunk && ch + nh > tree_ch) ||
-                                                  (TM == kTreeInCache && (ch + nh) * kChunk > L)));
-                    if (track) {
-                        // Sum the exact values and the rounding errors of the
-                        // bf16 values P.V will use (see the epilogue).
-                        float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int i = 0; i < KF; ++i) {
-                            const float e = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
-                            s[i] = __bfloat162float(__float2bfloat16_rn(e));
-                            sp[i & 7] += e;
-                            sr[i & 3] += s[i] - e;
-                        }
-                        l_err += (sr[0] + sr[1]) + (sr[2] + sr[3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < KF; ++i) {
-                            s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
-                            sp[i & 7] += s[i];
-                        }
+                    for (int i = 0; i < KF; ++i) {
+                        s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
+                        sp[i & 7] += s[i];
                     }
                     l_sum += ((sp[0] + sp[1]) + (sp[2] + sp[3])) +
                              ((sp[4] + sp[5]) + (sp[6] + sp[7]));
@@ -880,9 +867,19 @@ __global__ void __launch_bounds__(192, 1)
                 if (warp_any) {
                     const uint32_t tp = lane_base + S::TM_P + (jj & 1) * (kBlock / 2) + k0 / 2;
                     uint32_t pk[KF / 2];
+                    // With tracking, sum the rounding errors of the bf16 values
+                    // P.V will use, while the pairs are packed (bf16(p) - p).
+                    float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int i = 0; i < KF / 2; ++i)
+                    for (int i = 0; i < KF / 2; ++i) {
                         pk[i] = row_ok ? pack_bf16(s[2 * i], s[2 * i + 1]) : 0u;
+                        if (track && row_ok) {
+                            sr[(2 * i) & 3] += __uint_as_float(pk[i] << 16) - s[2 * i];
+                            sr[(2 * i + 1) & 3] +=
+                                __uint_as_float(pk[i] & 0xffff0000u) - s[2 * i + 1];
+                        }
+                    }
+                    if (track && row_ok) l_err += (sr[0] + sr[1]) + (sr[2] + sr[3]);
                     if constexpr (KF / 2 >= 32) {
 #pragma unroll
                         for (int c = 0; c < KF / 2; c += 32)
