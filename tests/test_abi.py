@@ -1,5 +1,6 @@
 """The C ABI library: loads, exports every declared symbol, and rejects bad
 arguments on the host before touching the GPU (CPU only)."""
+import ctypes
 import os
 import re
 import subprocess
@@ -233,3 +234,23 @@ def test_verify_tree_host_checks(lib):
     args = list(base)
     args[10] = a + 4
     assert f(*args) == -3          # mask_out alignment
+
+
+def test_plan_info_layout_matches_the_header(tmp_path):
+    # The ctypes mirror of tree_attn_plan_info must have the C struct's size
+    # and field offsets (a field added on one side only would shift the rest).
+    from speculative_decoding_tree_split_gb300._lib import PlanInfo
+    fields = [name for name, _ in PlanInfo._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tree_attn.h"',
+             'int main(void) {', '  printf("%zu\\n", sizeof(tree_attn_plan_info));']
+    lines += [f'  printf("%zu\\n", offsetof(tree_attn_plan_info, {f}));' for f in fields]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(PlanInfo)] + [getattr(PlanInfo, f).offset for f in fields]
+    assert got == want
