@@ -254,3 +254,20 @@ def test_plan_info_layout_matches_the_header(tmp_path):
                                           check=True).stdout.split()]
     want = [ctypes.sizeof(PlanInfo)] + [getattr(PlanInfo, f).offset for f in fields]
     assert got == want
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    # Every prototype's parameter count equals the ctypes argtypes the binding
+    # declares for it (a parameter added on one side only would misalign the call).
+    text = ""
+    for f in sorted(os.listdir(HEADER_DIR)):
+        if f.endswith(".h"):
+            text += open(os.path.join(HEADER_DIR, f)).read()
+    protos = re.findall(r"TREE_ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", text)
+    assert len(protos) == len(declared_functions())
+    for name, params in protos:
+        params = " ".join(params.split())
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None, name
+        assert len(argtypes) == n, (name, len(argtypes), n)
