@@ -9,7 +9,7 @@ default layout it is one tree_attn_verify_tree call (the masks are built
 inside the suffix/merge kernel); --layout paged_tree / full_mask call
 tree_mask_build first.
 
-    python bench.py [--config llama8b] [--steps K] [--warmup W]
+    python bench.py [--config chain] [--steps K] [--warmup W]
     python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...
     python bench.py --impl reference     # the fp64 CPU oracle, timed alone
 
@@ -61,7 +61,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", choices=sorted(CONFIGS), default="llama8b")
+    p.add_argument("--config", choices=sorted(CONFIGS), default="chain",
+                   help="headline workload (default: the largest single-GPU one, the "
+                        "64-sequence chain)")
     p.add_argument("--layout", choices=["shared", "per_seq", "paged_tree", "full_mask"],
                    default="shared",
                    help="shared: one draft tree for the batch, tree K/V in their own buffers; "
@@ -78,6 +80,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-long-context", action="store_true",
+                   help="time only --config (default: also every other long-context "
+                        "workload, reported under long_context)")
     return p.parse_args()
 
 
@@ -310,6 +315,141 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU side
 # ---------------------------------------------------------------------------
+# Workloads whose prefix pass the >= 70 %-of-HBM target is defined on (the
+# 70B layer is reported beside them); each is timed in the same run as the
+# headline workload.
+LONG_CONTEXT = ("llama8b", "llama70b", "chain", "maverick")
+
+
+class StepBench:
+    """Device state and CUDA graphs of one workload: `step` is one pass of
+    the whole hot path, `prefix_only` the prefix-pass kernel alone."""
+
+    def __init__(self, ta, cfg, layout, dev, seed, K, W):
+        self.ta, self.cfg, self.layout, self.dev, self.K, self.W = ta, cfg, layout, dev, K, W
+        wl = make_layout_workload(cfg, layout, seed=seed)
+        self.wl = wl
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 132 * 1024 * 1024
+        self.kv_alloc = wl.k_pages.numel() * 2 * 2
+        R = max(2, math.ceil(4 * self.l2 / max(self.kv_alloc, 1)))
+        self.R = R
+        # resident inputs
+        self.parents = wl.parents.to(dev)
+        self.q = wl.q.to(dev)
+        self.bt = wl.block_table.to(dev)
+        self.sl = wl.seq_lens.to(dev)
+        self.tk = wl.tree_k.to(dev)
+        self.tv = wl.tree_v.to(dev)
+        self.kps = [wl.k_pages.to(dev) for _ in range(R)]
+        self.vps = [wl.v_pages.to(dev) for _ in range(R)]
+        self.mask = torch.empty(tuple(wl.parents.shape), dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(cfg.B, cfg.T, cfg.Hq, dtype=torch.float32, device=dev)
+        ws_bytes = ta.workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.T, 0, cfg.page)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if layout == "full_mask":
+            self.cols = ta.dense_cols_for(int(wl.seq_lens.max()) + cfg.T)
+            self.dense = torch.empty((cfg.B, cfg.T, self.cols), dtype=torch.uint8, device=dev)
+            self.key_lens = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+
+    def hot_path(self, par, q_, k_, v_, bt_, sl_, tk_, tv_):
+        """One pass of the whole path: masks, then tree attention."""
+        ta, cfg, wl = self.ta, self.cfg, self.wl
+        layout, mask, out, lse, ws, status = (self.layout, self.mask, self.out, self.lse,
+                                              self.ws, self.status)
+        if layout == "full_mask":
+            ta.mask_build(par, mask_out=mask, status=status)
+            ta.dense_mask_build(mask, sl_, cfg.T, self.cols, dense_out=self.dense,
+                                key_lens=self.key_lens, status=status)
+            ta.verify_dense(q_, k_, v_, bt_, self.key_lens, self.dense, out=out, lse=lse,
+                            workspace=ws, status=status, softmax_scale=wl.scale)
+        elif layout == "paged_tree":
+            ta.mask_build(par, mask_out=mask, status=status)
+            ta.verify_paged_tree(q_, k_, v_, bt_, sl_, mask, out=out, lse=lse, workspace=ws,
+                                 status=status, softmax_scale=wl.scale)
+        else:
+            # shared / per_seq: tree_mask_build + tree_attn_verify in one call
+            # (tree_attn_verify_tree): the ancestor masks are built inside the
+            # attention kernels and written out
+            ta.verify_tree(q_, k_, v_, bt_, sl_, tk_, tv_, par, mask_out=mask, out=out, lse=lse,
+                           workspace=ws, status=status, softmax_scale=wl.scale)
+
+    def step(self, r):
+        self.hot_path(self.parents, self.q, self.kps[r % self.R], self.vps[r % self.R], self.bt,
+                      self.sl, self.tk, self.tv)
+
+    def prefix_only(self, r):
+        ta, wl = self.ta, self.wl
+        k_, v_ = self.kps[r % self.R], self.vps[r % self.R]
+        if self.layout == "full_mask":   # the one-pass kernel has no separate entry
+            ta.verify_dense(self.q, k_, v_, self.bt, self.key_lens, self.dense, out=self.out,
+                            lse=self.lse, workspace=self.ws, status=self.status,
+                            softmax_scale=wl.scale)
+            return
+        ta.prefix_pass(self.q, k_, v_, self.bt, self.sl, self.ws, status=self.status,
+                       softmax_scale=wl.scale)
+
+    def prepare(self):
+        """Eager warm-up (also applies the kernels' shared-memory opt-in before
+        capture), then the CUDA graphs; each graph is launched once, untimed:
+        a graph's first launch uploads it to the device."""
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for r in range(max(self.W, 1)):
+                self.step(r)
+                self.prefix_only(r)
+        torch.cuda.synchronize()
+        self.check_status("warm-up")
+
+        def capture(fn, n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for r in range(n):
+                    fn(r)
+            return g
+
+        self.g_timed = capture(self.step, self.K)
+        self.g_warm = capture(self.step, max(self.W, 1))
+        self.g_prefix = capture(self.prefix_only, self.K)
+        self.g_timed.replay()
+        self.g_prefix.replay()
+        torch.cuda.synchronize()
+
+    def check_status(self, where):
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"{self.cfg.name}: device status {int(self.status.item())} "
+                               f"during {where}")
+
+    def warm(self, seconds):
+        """W warm-up steps, then replays for about `seconds` (clocks settle and
+        the sampler sees the GPU under load)."""
+        self.g_warm.replay()
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            self.g_warm.replay()
+            torch.cuda.synchronize()
+
+
+def timed_replay(graph, barrier):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    s.record()
+    graph.replay()
+    e.record()
+    torch.cuda.synchronize()
+    barrier()
+    return s.elapsed_time(e)
+
+
+def traffic_for(name, layout, sha):
+    rec = NCU_TRAFFIC.get(name) if layout == "shared" else None
+    return rec[1] if rec is not None and rec[0] == sha else None
+
+
 def run_ours(args):
     import speculative_decoding_tree_split_gb300 as ta
 
@@ -324,157 +464,97 @@ def run_ours(args):
 
     cfg = CONFIGS[args.config]
     layout = args.layout
-    wl = make_layout_workload(cfg, layout, seed=cfg.seed + rank)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 132 * 1024 * 1024
-    kv_alloc = wl.k_pages.numel() * 2 * 2
-    R = max(2, math.ceil(4 * l2 / max(kv_alloc, 1)))
-
-    # resident inputs
-    parents = wl.parents.to(dev)
-    q = wl.q.to(dev)
-    bt = wl.block_table.to(dev)
-    sl = wl.seq_lens.to(dev)
-    tk = wl.tree_k.to(dev)
-    tv = wl.tree_v.to(dev)
-    kps = [wl.k_pages.to(dev) for _ in range(R)]
-    vps = [wl.v_pages.to(dev) for _ in range(R)]
-    mask = torch.empty(tuple(wl.parents.shape), dtype=torch.int64, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(cfg.B, cfg.T, cfg.Hq, dtype=torch.float32, device=dev)
-    ws_bytes = ta.workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.T, 0, cfg.page)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    if layout == "full_mask":
-        cols = ta.dense_cols_for(int(wl.seq_lens.max()) + cfg.T)
-        dense = torch.empty((cfg.B, cfg.T, cols), dtype=torch.uint8, device=dev)
-        key_lens = torch.empty(cfg.B, dtype=torch.int32, device=dev)
-
-    def hot_path(par, q_, k_, v_, bt_, sl_, tk_, tv_):
-        """One pass of the whole path: masks, then tree attention."""
-        if layout == "full_mask":
-            ta.mask_build(par, mask_out=mask, status=status)
-            ta.dense_mask_build(mask, sl_, cfg.T, cols, dense_out=dense, key_lens=key_lens,
-                                status=status)
-            ta.verify_dense(q_, k_, v_, bt_, key_lens, dense, out=out, lse=lse, workspace=ws,
-                            status=status, softmax_scale=wl.scale)
-        elif layout == "per_seq":
-            # the masks are built inside the verify call (tree_attn_verify_tree)
-            ta.verify_tree(q_, k_, v_, bt_, sl_, tk_, tv_, par, mask_out=mask, out=out, lse=lse,
-                           workspace=ws, status=status, softmax_scale=wl.scale)
-        elif layout == "paged_tree":
-            ta.mask_build(par, mask_out=mask, status=status)
-            ta.verify_paged_tree(q_, k_, v_, bt_, sl_, mask, out=out, lse=lse, workspace=ws,
-                                 status=status, softmax_scale=wl.scale)
-        else:
-            # tree_mask_build + tree_attn_verify in one call: the ancestor
-            # masks are built inside the suffix/merge kernel and written out
-            ta.verify_tree(q_, k_, v_, bt_, sl_, tk_, tv_, par, mask_out=mask, out=out, lse=lse,
-                           workspace=ws, status=status, softmax_scale=wl.scale)
-
-    def step(r):
-        hot_path(parents, q, kps[r % R], vps[r % R], bt, sl, tk, tv)
-
-    def prefix_only(r):
-        if layout == "full_mask":   # the one-pass kernel has no separate entry: time the call
-            ta.verify_dense(q, kps[r % R], vps[r % R], bt, key_lens, dense, out=out, lse=lse,
-                            workspace=ws, status=status, softmax_scale=wl.scale)
-            return
-        ta.prefix_pass(q, kps[r % R], vps[r % R], bt, sl, ws, status=status,
-                       softmax_scale=wl.scale)
-
-    # eager warm-up (also sets the kernels' shared-memory opt-in before capture)
-    side = torch.cuda.Stream(dev)
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        for r in range(max(args.warmup, 1)):
-            step(r)
-            prefix_only(r)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during warm-up")
-
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for r in range(n):
-                fn(r)
-        return g
-
     K, W = args.steps, args.warmup
-    g_timed = capture(step, K)
-    g_warm = capture(step, max(W, 1))
-    g_prefix = capture(prefix_only, K)
+    main = StepBench(ta, cfg, layout, dev, cfg.seed + rank, K, W)
+    main.prepare()
+    # The other long-context workloads, timed in the same run (one layout and
+    # one K for all, so the figures compare).
+    others = []
+    if not args.no_long_context and args.path == "verify":
+        for name in LONG_CONTEXT:
+            if name != args.config:
+                b = StepBench(ta, CONFIGS[name], layout, dev, CONFIGS[name].seed + rank, K, W)
+                b.prepare()
+                others.append(b)
+    props = torch.cuda.get_device_properties(dev)
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    def timed(graph):
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        barrier()
-        s.record()
-        graph.replay()
-        e.record()
-        torch.cuda.synchronize()
-        barrier()
-        return s.elapsed_time(e)
-
-    # Each graph's first launch uploads it to the device: launch the timed
-    # graphs once, untimed, so that the timed replays hold only the steps.
-    g_timed.replay()
-    g_prefix.replay()
-    torch.cuda.synchronize()
-    # warm-up replays (W steps), then keep the GPU loaded ~1 s so the clock
-    # sampler sees the timed region's clocks, then the timed K steps.
-    g_warm.replay()
+    # clocks are sampled from the first warm-up replay to the last timed one
     sampler = ClockSampler(smi_gpu_id(props, local))
     if not args.no_clocks:
         sampler.start()
-    t_end = time.perf_counter() + (0.0 if args.no_clocks else 1.2)
-    while time.perf_counter() < t_end:
-        g_warm.replay()
-        torch.cuda.synchronize()
-    ms_total = timed(g_timed)
-    ms_prefix_total = timed(g_prefix)
+    main.warm(0.0 if args.no_clocks else 1.2)
+    ms_total = timed_replay(main.g_timed, barrier)
+    ms_prefix_total = timed_replay(main.g_prefix, barrier)
+    other_ms = []
+    for b in others:
+        b.warm(0.0 if args.no_clocks else 0.3)
+        other_ms.append((timed_replay(b.g_timed, barrier), timed_replay(b.g_prefix, barrier)))
     clocks = sampler.stop() if not args.no_clocks else None
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    main.check_status("the timed region")
+    for b in others:
+        b.check_status("the timed region")
 
     ms_step = ms_total / K
     ms_prefix = ms_prefix_total / K
     ms_step, ms_prefix = max_over_ranks([ms_step, ms_prefix], dev)
     # Run-to-run spread: the same K-step graph replayed five more times, each
     # timed alone.  Reported beside `value`, which is the one timed region above.
-    reps = sorted(max_over_ranks([timed(g_timed) / K for _ in range(5)], dev))
+    reps = sorted(max_over_ranks([timed_replay(main.g_timed, barrier) / K for _ in range(5)],
+                                 dev))
     spread = {"replays": len(reps), "us_per_step_min": reps[0] * 1e3,
               "us_per_step_median": reps[len(reps) // 2] * 1e3, "us_per_step_max": reps[-1] * 1e3}
     tokens_per_step = cfg.B * cfg.T * world
     value = tokens_per_step / (ms_step * 1e-3)
 
-    nbytes = algorithmic_bytes(wl)
+    nbytes = algorithmic_bytes(main.wl)
     peak, peak_src = measured_hbm_peak()
     achieved = nbytes["prefix_kernel"] / (ms_prefix * 1e-3) / 1e9
     sha = kernel_source_sha()
-    traffic = None
-    rec = NCU_TRAFFIC.get(args.config) if layout == "shared" else None
-    if rec is not None and rec[0] == sha:
-        traffic = rec[1]
+    traffic = traffic_for(args.config, layout, sha)
+
+    def long_context_entry(b, ms_s, ms_p):
+        nb = algorithmic_bytes(b.wl)
+        c = b.cfg
+        gbs = nb["prefix_kernel"] / (ms_p * 1e-3) / 1e9
+        call_gbs = nb["kv"] / (ms_s * 1e-3) / 1e9
+        return {"workload": workload_desc(c, layout), "us_per_call": ms_s * 1e3,
+                "tokens_per_s": c.B * c.T * world / (ms_s * 1e-3),
+                "prefix_kernel_us": ms_p * 1e3, "prefix_gbs": gbs,
+                "prefix_frac_of_measured": gbs / peak, "prefix_frac_of_8tbs": gbs / 8000.0,
+                "call_kv_gbs": call_gbs, "call_frac_of_measured": call_gbs / peak,
+                "algorithmic_bytes_per_prefix_launch": nb["prefix_kernel"],
+                "traffic": traffic_for(c.name, layout, sha)}
+
+    long_context = None
+    if others:
+        long_context = {args.config: long_context_entry(main, ms_step, ms_prefix)}
+        for b, (ms_s, ms_p) in zip(others, other_ms):
+            ms_s, ms_p = max_over_ranks([ms_s / K, ms_p / K], dev)
+            long_context[b.cfg.name] = long_context_entry(b, ms_s, ms_p)
+    for b in others:   # free their device memory before the end-to-end leg
+        del b.kps, b.vps
+    others.clear()
+    torch.cuda.empty_cache()
 
     # end to end through the public API: pinned host inputs -> device, the
     # step, out/lse -> pinned host, every step
     e2e = None
+    wl = main.wl
     if not args.no_e2e:
         host = dict(parents=wl.parents, q=wl.q, k=wl.k_pages, v=wl.v_pages, bt=wl.block_table,
                     sl=wl.seq_lens, tk=wl.tree_k, tv=wl.tree_v)
-        d = dict(parents=parents, q=q, k=kps[0], v=vps[0], bt=bt, sl=sl, tk=tk, tv=tv)
+        d = dict(parents=main.parents, q=main.q, k=main.kps[0], v=main.vps[0], bt=main.bt,
+                 sl=main.sl, tk=main.tk, tv=main.tv)
         if layout in ("paged_tree", "full_mask"):   # the tree K/V travel inside the pages
             del host["tk"], host["tv"]
         h = {k: v.pin_memory() for k, v in host.items()}
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h_out = torch.empty(main.out.shape, dtype=main.out.dtype).pin_memory()
+        h_lse = torch.empty(main.lse.shape, dtype=main.lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in h.values())
         d2h = h_out.numel() * 2 + h_lse.numel() * 4
         n_e2e = max(3, min(K, int(20e9 // max(h2d, 1))))
@@ -482,9 +562,10 @@ def run_ours(args):
         def e2e_step():
             for key in h:
                 d[key].copy_(h[key], non_blocking=True)
-            hot_path(d["parents"], d["q"], d["k"], d["v"], d["bt"], d["sl"], d["tk"], d["tv"])
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
+            main.hot_path(d["parents"], d["q"], d["k"], d["v"], d["bt"], d["sl"], d["tk"],
+                          d["tv"])
+            h_out.copy_(main.out, non_blocking=True)
+            h_lse.copy_(main.lse, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -514,13 +595,15 @@ def run_ours(args):
                "sample_1_core": f"{n1} tree tokens, {el1:.1f} s, one thread"}
 
     if rank == 0:
-        emit({
+        line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg, layout), "tokens_per_step_per_gpu": cfg.B * cfg.T,
-                       "l2": f"{R} rotating device copies of the KV cache "
-                             f"({R * kv_alloc / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB)",
+            "config": {"workload": workload_desc(cfg, layout),
+                       "tokens_per_step_per_gpu": cfg.B * cfg.T,
+                       "l2": f"{main.R} rotating device copies of the KV cache "
+                             f"({main.R * main.kv_alloc / 2**20:.0f} MiB > L2 "
+                             f"{main.l2 / 2**20:.0f} MiB)",
                        "parallelism": f"replicas x{world}", "timing": "one CUDA graph of the "
                        "K steps, CUDA events on the replay stream"},
             "us_per_call": ms_step * 1e3,
@@ -533,9 +616,13 @@ def run_ours(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes["prefix_kernel"],
                          "peak_source": peak_src, "kernel_sha": sha},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP[layout] * K,
+            "clocks": clocks, "e2e": e2e,
+            "gpu_launches": LAUNCHES_PER_STEP[layout] * K,
             "cpu_baseline": cpu, "spread": spread,
-        })
+        }
+        if long_context is not None:
+            line["long_context"] = long_context
+        emit(line)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

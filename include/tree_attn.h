@@ -426,7 +426,10 @@ TREE_ATTN_API int tree_attn_suffix_merge(const uint16_t *q, const int32_t *seq_l
  *     a batch of 1 with 8 KV heads and d = 128 on 152 SMs needs 10.6 MB.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
- *     any stream capture.  No call allocates or frees memory.
+ *     any stream capture.  A cudaDeviceReset destroys the array's address
+ *     with the context: the first call after a reset looks it up again, so
+ *     make that call outside a capture too.  No call allocates or frees
+ *     memory.
  *   - All calls share the one array and it keeps the previous call's
  *     contents; nothing in it needs to start at zero.  Calls that overlap on
  *     the GPU (e.g. on two streams at once) race on it and give wrong

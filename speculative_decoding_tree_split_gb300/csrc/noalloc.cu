@@ -2,6 +2,7 @@
 // may not allocate device memory (fixed-budget memory pools, engines that
 // forbid allocation after start-up).  The prefix pass's partial results go
 // to a scratch array compiled into the library instead of a caller workspace.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -20,20 +21,59 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+// Unique id of the CUDA context the cached address belongs to (0: unknown).
+// A device reset destroys the context and with it the array's address; the
+// next context gets a new id, so the address is then looked up again.
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call must not be inside a stream capture).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context, or 0 when it cannot be had.
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device.  Looked up on
+// the first call with a device current, and again only when that device's
+// context has changed since (after a cudaDeviceReset); neither call may be
+// inside a stream capture.
 cudaError_t scratch_for_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_ctx_id();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    const bool stale = ctx != 0 && g_scratch_ctx[dev] != 0 && ctx != g_scratch_ctx[dev];
+    if (g_scratch_ptr[dev] == nullptr || stale) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+        // the lookup made the runtime's context current if it was not yet
+        g_scratch_ctx[dev] = ctx != 0 ? ctx : current_ctx_id();
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;

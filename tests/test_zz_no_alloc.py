@@ -1,8 +1,8 @@
 """tree_attn_verify_noalloc: the entry point for callers that cannot allocate
 device memory (fixed-budget memory pools, engines that forbid cudaMalloc after
 start-up).  It must give the same results as tree_attn_verify with a caller
-workspace, call after call, although every call reuses the library's one
-built-in scratch array.
+workspace, and as the fp64 oracle, call after call, although every call
+reuses the library's one built-in scratch array.
 
 Kept in its own file, collected last, so a stop-at-first-failure run has
 already run every other test; it also passes when run alone.
@@ -57,7 +57,7 @@ CASES = [
 ]
 
 
-def test_noalloc_matches_verify_on_two_calls_in_a_row(lib):
+def test_noalloc_matches_verify_on_two_calls_in_a_row(lib, oracle):
     prepared = []
     for cfg, lens in CASES:
         wl, x = _inputs(cfg, lens)
@@ -77,6 +77,11 @@ def test_noalloc_matches_verify_on_two_calls_in_a_row(lib):
         assert int(status.item()) == 0
         err_o = (out.float() - ref_out.float()).abs().max().item()
         err_l = (lse - ref_lse).abs().max().item()
+        assert err_o <= OUT_TOL and err_l <= LSE_TOL, (wl.cfg.name, err_o, err_l)
+        # and every row against the fp64 oracle
+        want_o, want_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
+        err_o = np.abs(out.float().cpu().numpy() - want_o).max()
+        err_l = np.abs(lse.cpu().numpy() - want_l).max()
         assert err_o <= OUT_TOL and err_l <= LSE_TOL, (wl.cfg.name, err_o, err_l)
 
 
