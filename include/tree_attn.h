@@ -449,6 +449,30 @@ TREE_ATTN_API int tree_attn_verify_noalloc(const uint16_t *q, const uint16_t *k_
                                            int num_pages, float softmax_scale, int32_t *status,
                                            void *stream);
 
+/*
+ * tree_attn_set_wait_limit_ns -- limit of the prefix pass's internal waits.
+ *
+ * The prefix pass is a warp-specialised pipeline: a copy warp, an MMA warp
+ * and softmax warps hand tiles to one another through shared-memory
+ * barriers.  Every such wait is bounded: one that lasts longer than this
+ * limit (nanoseconds of the GPU's global timer) makes the kernel store
+ * TREE_ATTN_STATUS_TIMEOUT in *status, let its own copies and MMAs in flight
+ * finish, free its tensor memory and return, so the CUDA context stays
+ * usable (the call's out / lse are then unspecified).  The failure detection
+ * this supports is a status word read on the host, never a trap.
+ *
+ *   ns   the new limit; 0 restores TREE_ATTN_DEFAULT_WAIT_NS (2 s).
+ *
+ * Returns the previous limit.  Process-wide; read when a call is enqueued,
+ * so a CUDA graph keeps the value in force when it was captured.  A healthy
+ * pipeline wait lasts microseconds: a short limit serves watchdogs and tests
+ * of the timeout path (a call under a limit shorter than its waits reports
+ * the timeout).  Host only; makes no CUDA call.
+ */
+#define TREE_ATTN_DEFAULT_WAIT_NS 2000000000ull
+
+TREE_ATTN_API unsigned long long tree_attn_set_wait_limit_ns(unsigned long long ns);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 TREE_ATTN_API int tree_attn_version(void);
 

@@ -38,4 +38,6 @@ from ._lib import (  # noqa: F401
     accept_commit,
     version,
     workspace_size,
+    set_wait_limit_ns,
+    DEFAULT_WAIT_NS,
 )

@@ -54,6 +54,7 @@ EXPORTED = (
     "tree_attn_plan",
     "tree_attn_verify_tree",
     "tree_accept_commit",
+    "tree_attn_set_wait_limit_ns",
 )
 
 
@@ -136,6 +137,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_accept_commit.restype = i32
     lib.tree_attn_version.argtypes = []
     lib.tree_attn_version.restype = i32
+    lib.tree_attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.tree_attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -580,6 +583,16 @@ def suffix_merge(q, seq_lens, max_pages_per_seq: int, page_size: int, tree_k, tr
         _ptr(workspace), workspace.numel(), int(n_ctas), _stream_handle(stream))
     if rc != 0:
         raise TreeAttnError("tree_attn_suffix_merge", rc)
+
+
+DEFAULT_WAIT_NS = 2_000_000_000
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit (ns) of the prefix pass's internal pipeline waits for calls
+    enqueued from now on; 0 restores the default (2 s).  Returns the previous
+    limit.  A call whose wait runs out stores STATUS_TIMEOUT in its status."""
+    return int(load().tree_attn_set_wait_limit_ns(int(ns)))
 
 
 def version() -> int:

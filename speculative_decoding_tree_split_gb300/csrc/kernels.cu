@@ -154,7 +154,8 @@ struct PrefixShape {
     static constexpr int O_FREE = 2 * NS + 9;
     static constexpr int Q_FULL = 2 * NS + 10;
     static constexpr int DRAIN = 2 * NS + 11;
-    static constexpr int NBAR = 2 * NS + 12;
+    static constexpr int FOLD = 2 * NS + 12;  // softmax warps meet before the fold
+    static constexpr int NBAR = 2 * NS + 13;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
     // TMEM columns: O at [0, D); S[2] (fp32, 128 keys each) after it; P[2]
@@ -201,6 +202,9 @@ struct PrefixArgs {
     int parents_stride;
     uint64_t* mask_out;
     int ovh;  // overhead slots per unit on the work line
+    // Limit of every wait on another role of the CTA (ns of %globaltimer);
+    // past it the kernel reports TREE_ATTN_STATUS_TIMEOUT and winds down.
+    unsigned long long wait_ns;
 };
 
 // Kernel variants of the prefix pass: the tree modes of layout.h, plus the
@@ -286,11 +290,6 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     }
 }
 
-// Barrier among `count` threads (whole warps) on hardware barrier `id`.
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -345,6 +344,7 @@ __global__ void __launch_bounds__(192, 1)
         ptx::mbar_init(bar(S::O_FREE), 4);
         ptx::mbar_init(bar(S::Q_FULL), 4);
         ptx::mbar_init(bar(S::DRAIN), 1);
+        ptx::mbar_init(bar(S::FOLD), 4);
         misc->abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tm_k);
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(192, 1)
                     const int nh = min(2, sg.chunk_end - ch);  // 64-token steps in this block
                     const int s = jj % S::NS;
                     if (jj >= S::NS &&
-                        !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1)) {
+                        !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1, a.wait_ns)) {
                         fail();
                         ok = false;
                         break;
@@ -492,10 +492,12 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             if (!ok) {
-                // Let every copy still in flight land before the CTA exits.
+                // Let every copy still in flight land before the CTA exits
+                // (they complete on their own: no other role is waited for).
                 const uint32_t first = jj > S::NS ? jj - S::NS : 0;
                 for (uint32_t j = first; j < jj; ++j)
-                    (void)ptx::mbar_wait(bar(S::KV_FULL + j % S::NS), (j / S::NS) & 1);
+                    (void)ptx::mbar_wait(bar(S::KV_FULL + j % S::NS), (j / S::NS) & 1,
+                                         ptx::kDrainLimitNs);
             }
         }
     } else if (warp == 5) {
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             Segment sg;
             while (ok && w.next(sg)) {
-                if (!ptx::mbar_wait(bar(S::Q_FULL), kk & 1)) {
+                if (!ptx::mbar_wait(bar(S::Q_FULL), kk & 1, a.wait_ns)) {
                     fail();
                     break;
                 }
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(192, 1)
                     } else {
                         const uint64_t now = ptx::globaltimer();
                         if (t0 == 0) t0 = now;
-                        if (now - t0 > ptx::kWaitLimitNs || *abort_flag) {
+                        if (now - t0 > a.wait_ns || *abort_flag) {
                             ok = false;
                             break;
                         }
@@ -597,9 +599,10 @@ __global__ void __launch_bounds__(192, 1)
                 jj += n;
                 ++kk;
             }
-            // Every MMA issued above must finish before TMEM is released.
+            // Every MMA issued above must finish before TMEM is released
+            // (they read only landed tiles and written P: they complete).
             ptx::mma_commit(bar(S::DRAIN));
-            (void)ptx::mbar_wait(bar(S::DRAIN), 0);
+            (void)ptx::mbar_wait(bar(S::DRAIN), 0, ptx::kDrainLimitNs);
         }
     } else {
         // ================= softmax + epilogue warpgroup (warps 0-3)
@@ -614,7 +617,7 @@ __global__ void __launch_bounds__(192, 1)
         w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
                misc->x1, TM, a.T, a.ovh);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
-            const bool ok = ptx::mbar_wait(b, parity);
+            const bool ok = ptx::mbar_wait(b, parity, a.wait_ns);
             const bool all = __all_sync(kFull, ok && !*abort_flag);
             if (!ok) fail();
             return all;
@@ -980,7 +983,14 @@ __global__ void __launch_bounds__(192, 1)
                         stg_ml[(g * R + lr) * 2 + 1] = l_sum;
                     }
                 }
-                named_bar_sync(1, 128);
+                // The four warps meet on an mbarrier rather than bar.sync: a
+                // warp that gave up on an earlier wait never arrives, and
+                // this wait is bounded.  Used once per launch (phase 0).
+                if (lane == 0) ptx::mbar_arrive(bar(S::FOLD));
+                if (!wait_all(bar(S::FOLD), 0)) {
+                    ok = false;
+                    break;
+                }
                 // RU rows per warp at a time: their shared-memory reads are
                 // all issued before any is used.
                 constexpr int RU = 4 / F;
@@ -1605,6 +1615,7 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     pa.parents_stride = v.parents_stride;
     pa.mask_out = v.mask_out;
     pa.ovh = v.ovh;
+    pa.wait_ns = v.wait_ns;
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
     const CUtensorMap& ttk = *static_cast<const CUtensorMap*>(tmap_tk);

@@ -41,6 +41,7 @@ struct VerifyArgs {
     // kTreeNone leaves them to the merge kernel (two-pass form).
     int tmode;
     int ovh;  // overhead slots per unit on the work line (the kernel selector's)
+    unsigned long long wait_ns;  // limit of a pipeline wait in the prefix pass
 };
 
 // Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and

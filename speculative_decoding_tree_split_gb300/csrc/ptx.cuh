@@ -8,9 +8,12 @@
 namespace treeattn {
 namespace ptx {
 
-// Upper bound for any single pipeline wait before the kernel gives up and
-// reports TREE_ATTN_STATUS_TIMEOUT (nanoseconds of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Upper bound (nanoseconds of %globaltimer) for a kernel's wait on its own
+// copies and MMAs in flight after it has given up on its pipeline: those
+// always complete, so this limit only guards against a broken device.  The
+// limit of the pipeline waits themselves is a kernel argument (the host's
+// setting, TREE_ATTN_DEFAULT_WAIT_NS unless changed).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,13 +56,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// if it did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// if it did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -38,7 +38,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert ta.version() == 10000
+    assert ta.version() == 10100
 
 
 def test_only_declared_symbols_are_exported(lib):
@@ -271,3 +271,11 @@ def test_binding_argument_counts_match_the_header(lib):
         argtypes = getattr(lib, name).argtypes
         assert argtypes is not None, name
         assert len(argtypes) == n, (name, len(argtypes), n)
+
+
+def test_wait_limit_setting_is_host_only_and_restorable(lib):
+    # no CUDA call is made: this runs on a machine without a GPU
+    assert ta.set_wait_limit_ns(5000) == ta.DEFAULT_WAIT_NS
+    assert ta.set_wait_limit_ns(7) == 5000
+    assert ta.set_wait_limit_ns(0) == 7          # 0 restores the default
+    assert ta.set_wait_limit_ns(0) == ta.DEFAULT_WAIT_NS
