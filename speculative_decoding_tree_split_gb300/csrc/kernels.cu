@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict
 // sees 2*d/16 instructions.
 // ===========================================================================
 constexpr int kBlock = 2 * kChunk;  // keys per MMA block
+// Block tables of at most this many entries (B * max_pages) are staged in
+// shared memory by the plan, in the same round trip as the sequence lengths.
+constexpr int kSmallBt = 128;
 
 template <int D>
 struct PrefixShape {
@@ -157,7 +160,8 @@ struct PrefixShape {
     static constexpr int FOLD = 2 * NS + 12;  // softmax warps meet before the fold
     static constexpr int NBAR = 2 * NS + 13;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    static constexpr int OFF_SBT = OFF_MISC + 64;  // a small block table (kSmallBt entries)
+    static constexpr int SMEM_BYTES = OFF_SBT + kSmallBt * 4 + 1024;  // + alignment slack
     // TMEM columns: O at [0, D); S[2] (fp32, 128 keys each) after it; P[2]
     // (bf16 pairs, 64 columns each) after S.
     static constexpr int TM_O = 0;
@@ -172,11 +176,18 @@ struct PrefixShape {
 };
 
 struct PrefixMisc {
-    long long W, x0, x1, base0;
-    int b0;
     uint32_t tmem_base;
     int abort;
 };
+
+// This CTA's share of the work line: total length W, its range [x0, x1), the
+// sequence b0 holding x0, that sequence's base position and seq_lens[b0].
+struct CtaPlan {
+    long long W, x0, x1, base0;
+    int b0;
+    int32_t lraw0;
+};
+static_assert(sizeof(PrefixMisc) <= 64, "PrefixMisc fits its shared-memory slot");
 
 struct PrefixArgs {
     const int32_t* block_table;
@@ -226,8 +237,13 @@ constexpr int kL1Line = 128;  // bytes per L1 cache line
 // entry): their seq_lens are read in one round trip, all loads in flight.
 constexpr int kPlanRegs = 4;
 
-// Total work W and this CTA's starting sequence / base (warp 0, all lanes).
-__device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
+// Total work W and this CTA's range and starting sequence (one warp, every
+// lane gets the result).  Every warp of the CTA computes it for itself, so no
+// role waits for a hand-over: the loads of all warps go out together and
+// share their L1 lines.  When `sbt` is not null a block table of at most
+// kSmallBt entries is also copied there (shared memory), its loads issued
+// together with the sequence lengths'.
+__device__ CtaPlan compute_plan(const PrefixArgs& a, int lane, int32_t* sbt) {
     const int upb = a.Hkv * a.RB;
     auto len_of = [&](int32_t L_raw, bool report_bad) -> int {
         bool bad;
@@ -241,6 +257,16 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     for (int i = 0; i < kPlanRegs; ++i) {
         const int b = 32 * i + lane;
         lraw[i] = b < a.B ? a.seq_lens[b] : 0;
+    }
+    const int nbt = a.B * a.max_pages;
+    if (sbt != nullptr && nbt <= kSmallBt) {
+        int32_t e[kSmallBt / 32];
+#pragma unroll
+        for (int i = 0; i < kSmallBt / 32; ++i)
+            e[i] = 32 * i + lane < nbt ? a.block_table[32 * i + lane] : -1;
+#pragma unroll
+        for (int i = 0; i < kSmallBt / 32; ++i)
+            if (32 * i + lane < nbt) sbt[32 * i + lane] = e[i];
     }
     int nreg[kPlanRegs];
 #pragma unroll
@@ -258,6 +284,7 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
     const long long x1 = cta_start(blockIdx.x + 1, W, a.n_ctas);
     int b_start = 0;
     long long base0 = 0;
+    int32_t lraw0 = 0;
     if (x0 < x1) {
         long long run = 0;
         for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -276,18 +303,24 @@ __device__ void compute_plan(const PrefixArgs& a, int lane, PrefixMisc* misc) {
                 const int src = __ffs(m) - 1;
                 b_start = b0 + src;
                 base0 = run + __shfl_sync(kFull, excl, src);
+                int32_t lr = 0;
+#pragma unroll
+                for (int i = 0; i < kPlanRegs; ++i)
+                    if (b0 == 32 * i) lr = __shfl_sync(kFull, lraw[i], src);
+                lraw0 = b0 >= 32 * kPlanRegs ? a.seq_lens[b_start] : lr;
                 break;
             }
             run += __shfl_sync(kFull, incl, 31);
         }
     }
-    if (lane == 0) {
-        misc->W = W;
-        misc->x0 = x0;
-        misc->x1 = x1;
-        misc->b0 = b_start;
-        misc->base0 = base0;
-    }
+    CtaPlan pl;
+    pl.W = W;
+    pl.x0 = x0;
+    pl.x1 = x1;
+    pl.b0 = b_start;
+    pl.base0 = base0;
+    pl.lraw0 = lraw0;
+    return pl;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -356,12 +389,124 @@ __global__ void __launch_bounds__(192, 1)
     }
     // L2 policy of the K/V loads (reads no input, so it is made before the wait).
     const uint64_t pol = (warp == 4 && lane == 0) ? ptx::policy_evict_first() : 0ull;
+    // The barriers and the TMEM base are in place before any role starts.
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const int upb = a.Hkv * a.RB;
+    const bool small_bt = static_cast<long long>(a.B) * a.max_pages <= kSmallBt;
+    int32_t* sbt = reinterpret_cast<int32_t*>(smem + S::OFF_SBT);
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        report(a.status, TREE_ATTN_STATUS_TIMEOUT);
+    };
+
+    // Physical pages of block jj -- work-line steps ch and ch + 1 of segment
+    // sg: the block-table loads are only issued here (all at once), and used
+    // by issue_block, so the caller can wait for the ring in between.
+    struct BlockPages {
+        int pids[8];
+        bool use[8];
+    };
+    auto block_pages = [&](const Segment& sg, int ch, BlockPages& bp) {
+        bool bad;
+        const int L = clamp_seq_len(sg.len_raw, a.P, a.max_pages, bad);
+        // Pages holding this unit's keys: the prefix, and for kTreeInCache
+        // the tree tokens padded after it.
+        int npages = (L + a.P - 1) / a.P;
+        if (TM == kTreeInCache) npages = min(a.max_pages, (L + a.T + a.P - 1) / a.P);
+        const int tree_ch = chunks_of(L);
+        const int Pb = a.P < kChunk ? a.P : kChunk;
+        const int nsub = kChunk / Pb;
+        const int pshift = __ffs(a.P) - 1;
+        const size_t row = static_cast<size_t>(sg.b) * a.max_pages;
+        const int nh = min(2, sg.chunk_end - ch);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = hh * 4 + i;
+                const int tok = (ch + hh) * kChunk + i * Pb;
+                const int lp = tok >> pshift;
+                bp.use[k] = hh < nh && i < nsub && lp < npages &&
+                            !(TM == kTreeChunk && ch + hh == tree_ch);
+                bp.pids[k] = bp.use[k] ? (small_bt ? sbt[row + lp] : a.block_table[row + lp]) : -1;
+            }
+        }
+    };
+    // Issues the K/V loads of block jj (pages from block_pages) into ring
+    // stage jj % NS, which the caller has found free.
+    auto issue_block = [&](const Segment& sg, int ch, uint32_t jj, const BlockPages& bp) {
+        bool bad;
+        const int L = clamp_seq_len(sg.len_raw, a.P, a.max_pages, bad);
+        const int tree_ch = chunks_of(L);            // the tree chunk (kTreeChunk)
+        const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
+        const int nh = min(2, sg.chunk_end - ch);    // 64-token steps in this block
+        const int s = jj % S::NS;
+        int ys[8];
+        int rows[8];
+        int nl = 0;
+        int tree_half = -1;  // half of the block holding the tree chunk
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            if (TM == kTreeChunk && hh < nh && ch + hh == tree_ch) tree_half = hh;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = hh * 4 + i;
+                if (!bp.use[k]) continue;
+                const int pid = bp.pids[k];
+                if (pid < 0 || pid >= a.num_pages) {
+                    report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
+                    continue;
+                }
+                const int tok = (ch + hh) * kChunk + i * Pb;
+                ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok & (a.P - 1));
+                rows[nl] = hh * kChunk + i * Pb;
+                ++nl;
+            }
+        }
+        const uint32_t fb = bar(S::KV_FULL + s);
+        // a tree chunk is one 64-row box per 64 columns of K and of V
+        const uint32_t bytes =
+            static_cast<uint32_t>((nl * Pb + (tree_half >= 0 ? kChunk : 0)) * 128 * S::DH * 2);
+        if (bytes != 0) {
+            ptx::mbar_arrive_expect_tx(fb, bytes);
+        } else {
+            ptx::mbar_arrive(fb);
+        }
+        const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
+        const uint32_t vst = kst + S::TILE_BYTES;
+#pragma unroll 1
+        for (int l = 0; l < nl; ++l) {
+#pragma unroll
+            for (int h = 0; h < S::DH; ++h) {
+                ptx::tma_load_2d(kst + h * S::HALF_BYTES + rows[l] * 128, &tm_k, h * 64, ys[l], fb,
+                                 pol);
+                ptx::tma_load_2d(vst + h * S::HALF_BYTES + rows[l] * 128, &tm_v, h * 64, ys[l], fb,
+                                 pol);
+            }
+        }
+        if (TM == kTreeChunk && tree_half >= 0) {
+            // Tree tokens 0..63 of (b, hk): rows b*T + j of the [B*T][Hkv][d]
+            // buffers (rows past the tree are other sequences' tokens or zero
+            // fill; they are masked and their V rows zeroed).
+#pragma unroll
+            for (int h = 0; h < S::DH; ++h) {
+                const uint32_t off = h * S::HALF_BYTES + tree_half * kChunk * 128;
+                ptx::tma_load_3d(kst + off, &tm_tk, h * 64, sg.hk, sg.b * a.T, fb, pol);
+                ptx::tma_load_3d(vst + off, &tm_tv, h * 64, sg.hk, sg.b * a.T, fb, pol);
+            }
+        }
+    };
+
     // Inputs may come from the kernel before us in the stream.
     ptx::grid_dep_wait();
-    if (warp == 0) compute_plan(a, lane, misc);
-    if (warp == 4) {
-        // A small block table is pulled into L1 while the plan is computed, so
-        // the producer's first page lookups do not each wait for L2.
+    const CtaPlan pl = compute_plan(a, lane, warp == 4 && small_bt ? sbt : nullptr);
+    if (warp == 4 && small_bt) __syncwarp();  // the staged table is visible to lane 0
+    if (warp == 4 && !small_bt) {
+        // A block table of a few lines is pulled into L1 while the producer
+        // starts, so its first page lookups do not each wait for L2.
         const long long lines =
             (static_cast<long long>(a.B) * a.max_pages * 4 + kL1Line - 1) / kL1Line;
         if (lines <= 2 * 32) {
@@ -370,42 +515,28 @@ __global__ void __launch_bounds__(192, 1)
             if (lane + 32 < lines) ptx::prefetch_l1(bt + static_cast<size_t>(lane + 32) * kL1Line);
         }
     }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
     ptx::grid_dep_launch();
     const uint32_t tmem = misc->tmem_base;
-    const int upb = a.Hkv * a.RB;
-
-    auto fail = [&]() {
-        *abort_flag = 1;
-        report(a.status, TREE_ATTN_STATUS_TIMEOUT);
+    auto init_walker = [&](Walker& w) {
+        w.init_known(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, pl.b0, pl.base0, pl.x0, pl.x1,
+                     TM, a.T, a.ovh, pl.lraw0);
     };
 
     if (warp == 4) {
         // ================= TMA producer (one thread)
         if (lane == 0) {
             Walker w;
-            w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1, TM, a.T, a.ovh);
-            const int Pb = a.P < kChunk ? a.P : kChunk;  // rows per TMA box
-            const int nsub = kChunk / Pb;                // boxes per 64-token step
-            const int pshift = __ffs(a.P) - 1;           // page_size is a power of two
+            init_walker(w);
             uint32_t jj = 0;
             bool ok = true;
             Segment sg;
             while (ok && w.next(sg)) {
-                bool bad;
-                const int L = clamp_seq_len(sg.len_raw, a.P, a.max_pages, bad);
-                // Pages holding this unit's keys: the prefix, and for
-                // kTreeInCache the tree tokens padded after it.
-                int npages = (L + a.P - 1) / a.P;
-                if (TM == kTreeInCache) npages = min(a.max_pages, (L + a.T + a.P - 1) / a.P);
-                const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
-                const int32_t* bt = a.block_table + static_cast<size_t>(sg.b) * a.max_pages;
 #pragma unroll 1
                 for (int ch = sg.chunk_begin; ch < sg.chunk_end; ch += 2, ++jj) {
-                    const int nh = min(2, sg.chunk_end - ch);  // 64-token steps in this block
+                    // The block's page lookups go out before the wait for its
+                    // ring stage, so their round trip overlaps that wait.
+                    BlockPages bp;
+                    block_pages(sg, ch, bp);
                     const int s = jj % S::NS;
                     if (jj >= S::NS &&
                         !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1, a.wait_ns)) {
@@ -417,78 +548,7 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
-                    // Pages of this block (at most 2 steps x 4 boxes): every
-                    // block-table load is issued before any is used, so a block
-                    // costs one round trip to the table, not one per page.
-                    int pids[8];
-                    bool use[8];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int k = hh * 4 + i;
-                            const int tok = (ch + hh) * kChunk + i * Pb;
-                            const int lp = tok >> pshift;
-                            use[k] = hh < nh && i < nsub && lp < npages &&
-                                     !(TM == kTreeChunk && ch + hh == tree_ch);
-                            pids[k] = use[k] ? bt[lp] : -1;
-                        }
-                    }
-                    int ys[8];
-                    int rows[8];
-                    int nl = 0;
-                    int tree_half = -1;  // half of the block holding the tree chunk
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (TM == kTreeChunk && hh < nh && ch + hh == tree_ch) tree_half = hh;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int k = hh * 4 + i;
-                            if (!use[k]) continue;
-                            const int pid = pids[k];
-                            if (pid < 0 || pid >= a.num_pages) {
-                                report(a.status, TREE_ATTN_STATUS_BAD_PAGE);
-                                continue;
-                            }
-                            const int tok = (ch + hh) * kChunk + i * Pb;
-                            ys[nl] = (pid * a.Hkv + sg.hk) * a.P + (tok & (a.P - 1));
-                            rows[nl] = hh * kChunk + i * Pb;
-                            ++nl;
-                        }
-                    }
-                    const uint32_t fb = bar(S::KV_FULL + s);
-                    // a tree chunk is one 64-row box per 64 columns of K and of V
-                    const uint32_t bytes = static_cast<uint32_t>(
-                        (nl * Pb + (tree_half >= 0 ? kChunk : 0)) * 128 * S::DH * 2);
-                    if (bytes != 0) {
-                        ptx::mbar_arrive_expect_tx(fb, bytes);
-                    } else {
-                        ptx::mbar_arrive(fb);
-                    }
-                    const uint32_t kst = sb + S::OFF_STAGE + s * S::STAGE_BYTES;
-                    const uint32_t vst = kst + S::TILE_BYTES;
-#pragma unroll 1
-                    for (int l = 0; l < nl; ++l) {
-#pragma unroll
-                        for (int h = 0; h < S::DH; ++h) {
-                            ptx::tma_load_2d(kst + h * S::HALF_BYTES + rows[l] * 128, &tm_k, h * 64,
-                                             ys[l], fb, pol);
-                            ptx::tma_load_2d(vst + h * S::HALF_BYTES + rows[l] * 128, &tm_v, h * 64,
-                                             ys[l], fb, pol);
-                        }
-                    }
-                    if (TM == kTreeChunk && tree_half >= 0) {
-                        // Tree tokens 0..63 of (b, hk): rows b*T + j of the
-                        // [B*T][Hkv][d] buffers (rows past the tree are other
-                        // sequences' tokens or zero fill; they are masked and
-                        // their V rows zeroed).
-#pragma unroll
-                        for (int h = 0; h < S::DH; ++h) {
-                            const uint32_t off = h * S::HALF_BYTES + tree_half * kChunk * 128;
-                            ptx::tma_load_3d(kst + off, &tm_tk, h * 64, sg.hk, sg.b * a.T, fb, pol);
-                            ptx::tma_load_3d(vst + off, &tm_tv, h * 64, sg.hk, sg.b * a.T, fb, pol);
-                        }
-                    }
+                    issue_block(sg, ch, jj, bp);
                 }
             }
             if (!ok) {
@@ -507,8 +567,7 @@ __global__ void __launch_bounds__(192, 1)
         // comes first, so neither waits behind the other.
         if (lane == 0) {
             Walker w;
-            w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-                   misc->x1, TM, a.T, a.ovh);
+            init_walker(w);
             const uint32_t idesc_qk = idesc_bf16_f32(kRows, kBlock, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, D, false, true);
             uint32_t jj = 0, kk = 0;  // blocks of earlier segments, segments done
@@ -610,12 +669,24 @@ __global__ void __launch_bounds__(192, 1)
         constexpr int KF = kBlock / F;  // keys of each block one replica handles
         const int r = threadIdx.x;      // tile row == TMEM lane
         const int g = r / R;            // replica of this row (warp-uniform)
-        const int lr = r % R;           // query row within the row block
+        const int lt = r % R;           // tile row within the replica
         const int k0 = g * KF;          // first key of this replica in a block
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Query row of tile row lt when the row block holds Mrb query rows
+        // (R when none).  A warp reaches only its own 32 TMEM lanes, and the
+        // four warps run on the SM's four sub-partitions, so the rows are
+        // spread evenly over the replica's 32-lane groups: with 80 rows and
+        // one replica each group takes 20 and every sub-partition computes
+        // 20 rows' exponentials, instead of 32, 32, 16 and 0.
+        auto query_row = [&](int Mrb) -> int {
+            constexpr int groups = R / 32;
+            const int per = (Mrb + groups - 1) / groups;
+            const int within = lt & 31;
+            const int q = (lt >> 5) * per + within;
+            return (within < per && q < Mrb) ? q : R;
+        };
         Walker w;
-        w.init(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, misc->b0, misc->base0, misc->x0,
-               misc->x1, TM, a.T, a.ovh);
+        init_walker(w);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
             const bool ok = ptx::mbar_wait(b, parity, a.wait_ns);
             const bool all = __all_sync(kFull, ok && !*abort_flag);
@@ -636,9 +707,10 @@ __global__ void __launch_bounds__(192, 1)
         // replica gets a copy).
         auto load_q = [&](const Segment& sg) {
             const int Mrb = min(R, a.M - sg.rb * kRows);
+            const int lq = query_row(Mrb);
             uint8_t* qs = smem + S::OFF_Q;
-            if (lr < Mrb) {
-                const int rr = sg.rb * kRows + lr;
+            if (lq < Mrb) {
+                const int rr = sg.rb * kRows + lq;
                 const int t = rr / a.G, gg = rr % a.G;
                 const int h = sg.hk * a.G + gg;
                 const uint4* src = reinterpret_cast<const uint4*>(
@@ -667,8 +739,10 @@ __global__ void __launch_bounds__(192, 1)
         if (have) load_q(cur);
         while (ok && have) {
             const int Mrb = min(R, a.M - cur.rb * kRows);
+            const int lr = query_row(Mrb);  // query row within the row block
             const bool row_ok = lr < Mrb;
-            const bool warp_any = (warp * 32) % R < Mrb;
+            const bool warp_any = __any_sync(kFull, row_ok);
+            const int prow = g * R + lr;    // row of this copy's partial in a slot
             bool bad;
             const int L = clamp_seq_len(cur.len_raw, a.P, a.max_pages, bad);
             const int tree_ch = chunks_of(L);  // the tree chunk (kTreeChunk)
@@ -1060,7 +1134,7 @@ __global__ void __launch_bounds__(192, 1)
                 // stores its own partial (hidden behind the next segment's
                 // loads, which are already in flight).
                 float4* acc =
-                    reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(r) * D);
+                    reinterpret_cast<float4*>(slot + 2 * kRows + static_cast<size_t>(prow) * D);
 #pragma unroll
                 for (int c = 0; c < D; c += 32) {
                     float o[32];
@@ -1078,8 +1152,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 if (row_ok) {
-                    slot[r] = m_ref;
-                    slot[kRows + r] = l_sum;
+                    slot[prow] = m_ref;
+                    slot[kRows + prow] = l_sum;
                 }
             }
             ptx::tc_fence_before();

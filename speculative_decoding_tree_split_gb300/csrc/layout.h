@@ -190,6 +190,14 @@ struct Walker {
     TA_HD void init(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
                     long long base0, long long x0, long long x1_, int tmode_ = kTreeNone,
                     int T_ = 0, int ovh_ = 0) {
+        init_known(sl, B_, P_, maxp, upb, RB_, b0, base0, x0, x1_, tmode_, T_, ovh_,
+                   (x0 < x1_) ? sl[b0] : 0);
+    }
+
+    // As init, with seq_lens[b0] already known (read by the caller's plan).
+    TA_HD void init_known(const int32_t* sl, int B_, int P_, int maxp, int upb, int RB_, int b0,
+                          long long base0, long long x0, long long x1_, int tmode_, int T_,
+                          int ovh_, int32_t lraw_b0) {
         tmode = tmode_;
         T = T_;
         ovh = ovh_;
@@ -204,7 +212,12 @@ struct Walker {
         x = x0;
         x1 = x1_;
         lraw = 0;
-        nch = (x0 < x1_) ? chunks_b(b0) : 0;
+        nch = 0;
+        if (x0 < x1_) {
+            bool bad;
+            lraw = lraw_b0;
+            nch = unit_chunks(lraw_b0, P, max_pages, tmode, T, bad);
+        }
         len = unit_len(nch, ovh);
     }
 
