@@ -50,8 +50,11 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel from an ncu capture, keyed by workload, valid only for the kernel
 # source whose SHA-256 is recorded with it (see profiles/).
 NCU_TRAFFIC = {
-    # Llama-3.1-8B layer, mean of three launches of one ncu capture
-    "llama8b": ("402ec8fece82c130", 33736874),
+    # profiles/prefix_pass_traffic_long_context.md
+    "chain": ("3b028dafdeaf8627", 2376678144),
+    "maverick": ("3b028dafdeaf8627", 541116160),
+    "llama70b": ("3b028dafdeaf8627", 339200000),
+    "llama8b": ("3b028dafdeaf8627", 33735936),
 }
 
 
