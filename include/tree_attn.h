@@ -473,6 +473,39 @@ TREE_ATTN_API int tree_attn_verify_noalloc(const uint16_t *q, const uint16_t *k_
 
 TREE_ATTN_API unsigned long long tree_attn_set_wait_limit_ns(unsigned long long ns);
 
+/* Early start of the prefix pass (an opt-in promise about the stream).
+ *
+ * Every kernel of this library is launched with programmatic dependent
+ * launch: its CTAs may start while the kernel before it in the stream is
+ * still running, and wait for that kernel (griddepcontrol.wait) before they
+ * read an input it may write.  By default the prefix pass waits before it
+ * reads anything.
+ *
+ * Enabling this setting is the caller's promise that the kernel directly
+ * before each later call in its stream writes none of seq_lens,
+ * block_table and the committed-prefix rows of k_pages / v_pages (the
+ * usual case: that kernel produces q and the tree tokens' K/V).  The prefix
+ * pass then plans its work and issues the loads of its first ring stages of
+ * committed-prefix K/V before that wait, overlapping them with the previous
+ * kernel's tail; q, the tree K/V (also when padded into the paged cache),
+ * the parent array and the masks are still read after the wait, and the
+ * workspace is written only after it.  The one-pass explicit-mask form
+ * (tree_attn_verify_dense) ignores the setting.  Results are the same
+ * either way; a call whose promise does not hold may read stale prefix
+ * data.  (Copies and memsets before a kernel complete before it starts
+ * whatever the setting.  This library's kernels let their successor start
+ * only after their own wait for the kernel before them; a kernel of the
+ * caller's that signals its successor before its own wait extends the
+ * promise to the kernels it may overlap.)
+ *
+ *   enable   non-zero to enable, 0 to disable (the default).
+ *
+ * Returns the previous setting (0 or 1).  Process-wide; read when a call is
+ * enqueued, so a CUDA graph keeps the value in force when it was captured.
+ * Host only; makes no CUDA call.
+ */
+TREE_ATTN_API int tree_attn_set_early_prefix_loads(int enable);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 TREE_ATTN_API int tree_attn_version(void);
 

@@ -39,5 +39,6 @@ from ._lib import (  # noqa: F401
     version,
     workspace_size,
     set_wait_limit_ns,
+    set_early_prefix_loads,
     DEFAULT_WAIT_NS,
 )

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreeattn.so")
-SOURCES = ["kernels.cu", "tree_attn.cu", "noalloc.cu", "accept.cu"]
+SOURCES = ["kernels.cu", "prefix_early.cu", "tree_attn.cu", "noalloc.cu", "accept.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I" + INCLUDE]

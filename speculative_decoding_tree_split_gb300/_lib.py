@@ -55,6 +55,7 @@ EXPORTED = (
     "tree_attn_verify_tree",
     "tree_accept_commit",
     "tree_attn_set_wait_limit_ns",
+    "tree_attn_set_early_prefix_loads",
 )
 
 
@@ -139,6 +140,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tree_attn_version.restype = i32
     lib.tree_attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.tree_attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    lib.tree_attn_set_early_prefix_loads.argtypes = [i32]
+    lib.tree_attn_set_early_prefix_loads.restype = i32
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -593,6 +596,14 @@ def set_wait_limit_ns(ns: int) -> int:
     enqueued from now on; 0 restores the default (2 s).  Returns the previous
     limit.  A call whose wait runs out stores STATUS_TIMEOUT in its status."""
     return int(load().tree_attn_set_wait_limit_ns(int(ns)))
+
+
+def set_early_prefix_loads(enable: bool) -> bool:
+    """Promise, for calls enqueued from now on, that the kernel before each
+    call in its stream writes none of seq_lens, block_table and the committed
+    prefix K/V: the prefix pass then plans and loads its first K/V blocks
+    before waiting for that kernel.  Returns the previous setting."""
+    return bool(load().tree_attn_set_early_prefix_loads(1 if enable else 0))
 
 
 def version() -> int:

@@ -11,7 +11,8 @@
 //
 // Both kernels are latency-bound (a few KB per sequence); they take part in
 // programmatic dependent launch so that they overlap the previous kernel's
-// tail.
+// tail.  Each lets the next kernel start only after its own wait for the
+// kernel before, so no successor runs beside a kernel older than this one.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -114,8 +115,8 @@ __global__ void __launch_bounds__(32 * kAcceptWarps)
                          const int32_t* __restrict__ draft, const int32_t* __restrict__ target,
                          int B, int T, int32_t* __restrict__ accept_len,
                          int32_t* __restrict__ accept_path, int32_t* __restrict__ bonus) {
-    ptx::grid_dep_launch();
     ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
     if (b >= B) return;
@@ -230,8 +231,8 @@ __device__ __forceinline__ void commit_rows(const CommitArgs& a, int b, int hk, 
 }
 
 __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(CommitArgs a) {
-    ptx::grid_dep_launch();
     ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     const int b = blockIdx.x;
     commit_rows(a, b, blockIdx.y, a.accept_len[b], a.accept_path + static_cast<size_t>(b) * a.T);
 }
@@ -251,8 +252,8 @@ struct AcceptArgs {
 
 __global__ void __launch_bounds__(kCommitThreads)
     accept_commit_kernel(CommitArgs a, AcceptArgs g) {
-    ptx::grid_dep_launch();
     ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     __shared__ int32_t path[TREE_ATTN_MAX_T];
     __shared__ int n_s;
     const int b = blockIdx.x, hk = blockIdx.y;

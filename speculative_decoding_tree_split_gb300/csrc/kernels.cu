@@ -99,16 +99,18 @@ __device__ __forceinline__ bool warp_tree_mask(const int32_t* parents, int T, in
     return __any_sync(kFull, bad);
 }
 
+#ifndef TREE_ATTN_EARLY_TU
 __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict__ parents, int T,
                                                        uint64_t* __restrict__ mask,
                                                        int32_t* status) {
     // CTA b builds the mask of tree b (a batch of trees is [B][T]).
     parents += static_cast<size_t>(blockIdx.x) * T;
     mask += static_cast<size_t>(blockIdx.x) * T;
-    // The next kernel may start its prologue now; it waits for this grid
-    // before reading anything this grid writes.
-    ptx::grid_dep_launch();
+    // Wait for the kernel before; only then may the next kernel start (it
+    // waits for this grid before reading anything this grid writes), so no
+    // successor ever runs beside a kernel older than this one.
     ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     const int lane = threadIdx.x;
     uint64_t anc[2];
     if (warp_tree_mask(parents, T, lane, anc) && lane == 0)
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(32) tree_mask_kernel(const int32_t* __restrict
         if (i < T) mask[i] = anc[h];
     }
 }
+#endif  // !TREE_ATTN_EARLY_TU
 
 // ===========================================================================
 // Prefix pass
@@ -133,6 +136,11 @@ constexpr int kBlock = 2 * kChunk;  // keys per MMA block
 // Block tables of at most this many entries (B * max_pages) are staged in
 // shared memory by the plan, in the same round trip as the sequence lengths.
 constexpr int kSmallBt = 128;
+// Early start: K/V blocks a CTA loads before its dependency wait.  The plan
+// and the first block's page lookups always go first; each block loaded
+// early also takes memory bandwidth from the tail of the kernel before.
+constexpr int kEarlyBlocks = 3;
+static_assert(kEarlyBlocks <= 3, "early blocks go to ring stages that need no release");
 
 template <int D>
 struct PrefixShape {
@@ -341,7 +349,12 @@ __device__ __forceinline__ int blocks_of(const Segment& sg) {
     return (sg.chunk_end - sg.chunk_begin + 1) / 2;
 }
 
-template <int D, int F, int MODE>
+// EARLY: seq_lens, block_table and the committed prefix K/V are not written
+// by the kernel before this one in the stream, so the plan and the first ring
+// stages' loads of committed-prefix blocks go out before the dependency wait
+// (q, the tree K/V and the masks are read after it).  The explicit-mask form
+// has no early variant.
+template <int D, int F, int MODE, bool EARLY>
 __global__ void __launch_bounds__(192, 1)
     prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -435,6 +448,17 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     };
+    // Whether block (sg, ch) holds committed-prefix keys only, i.e. reads no
+    // tree K/V (kTreeChunk: the tree chunk; kTreeInCache: the pages past the
+    // prefix, where the tree tokens are written).
+    auto committed_block = [&](const Segment& sg, int ch) -> bool {
+        bool bad;
+        const int L = clamp_seq_len(sg.len_raw, a.P, a.max_pages, bad);
+        const int nh = min(2, sg.chunk_end - ch);
+        if (TM == kTreeInCache) return static_cast<long long>(ch + nh) * kChunk <= L;
+        if (TM == kTreeChunk) return ch + nh <= chunks_of(L);
+        return true;
+    };
     // Issues the K/V loads of block jj (pages from block_pages) into ring
     // stage jj % NS, which the caller has found free.
     auto issue_block = [&](const Segment& sg, int ch, uint32_t jj, const BlockPages& bp) {
@@ -500,8 +524,12 @@ __global__ void __launch_bounds__(192, 1)
         }
     };
 
-    // Inputs may come from the kernel before us in the stream.
-    ptx::grid_dep_wait();
+    // Inputs may come from the kernel before us in the stream.  Under EARLY
+    // the plan's inputs do not, and each role waits where it first reads one
+    // that may (the producer before its first block that is not committed
+    // prefix or does not fit the ring; the softmax warps before Q).
+    constexpr bool early = EARLY && !DENSE;
+    if (!early) ptx::grid_dep_wait();
     const CtaPlan pl = compute_plan(a, lane, warp == 4 && small_bt ? sbt : nullptr);
     if (warp == 4 && small_bt) __syncwarp();  // the staged table is visible to lane 0
     if (warp == 4 && !small_bt) {
@@ -515,7 +543,11 @@ __global__ void __launch_bounds__(192, 1)
             if (lane + 32 < lines) ptx::prefetch_l1(bt + static_cast<size_t>(lane + 32) * kL1Line);
         }
     }
-    ptx::grid_dep_launch();
+    // The next kernel may start once every CTA has passed here; it reads, before
+    // its own dependency wait, inputs of the kernel before us (the merge reads
+    // q, the tree K/V and the parents), so under EARLY the signal is given
+    // only after this CTA has waited for that kernel (softmax warps, below).
+    if (!early) ptx::grid_dep_launch();
     const uint32_t tmem = misc->tmem_base;
     auto init_walker = [&](Walker& w) {
         w.init_known(a.seq_lens, a.B, a.P, a.max_pages, upb, a.RB, pl.b0, pl.base0, pl.x0, pl.x1,
@@ -529,6 +561,7 @@ __global__ void __launch_bounds__(192, 1)
             init_walker(w);
             uint32_t jj = 0;
             bool ok = true;
+            bool dep_done = !early;  // the dependency wait is behind this thread
             Segment sg;
             while (ok && w.next(sg)) {
 #pragma unroll 1
@@ -537,6 +570,10 @@ __global__ void __launch_bounds__(192, 1)
                     // ring stage, so their round trip overlaps that wait.
                     BlockPages bp;
                     block_pages(sg, ch, bp);
+                    if (!dep_done && (jj >= kEarlyBlocks || !committed_block(sg, ch))) {
+                        ptx::grid_dep_wait();
+                        dep_done = true;
+                    }
                     const int s = jj % S::NS;
                     if (jj >= S::NS &&
                         !ptx::mbar_wait(bar(S::KV_EMPTY + s), ((jj / S::NS) - 1) & 1, a.wait_ns)) {
@@ -685,6 +722,10 @@ __global__ void __launch_bounds__(192, 1)
             const int q = (lt >> 5) * per + within;
             return (within < per && q < Mrb) ? q : R;
         };
+        if constexpr (early) {
+            ptx::grid_dep_wait();  // Q and the tree inputs may be the previous kernel's
+            ptx::grid_dep_launch();
+        }
         Walker w;
         init_walker(w);
         auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
@@ -1175,6 +1216,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+#ifndef TREE_ATTN_EARLY_TU
 // ===========================================================================
 // Suffix pass + merge.  One warp per query row; lane l holds elements
 // [l*E, l*E + E) of the head dimension.
@@ -1624,6 +1666,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
     }
 }
 
+#endif  // !TREE_ATTN_EARLY_TU
+
 template <typename Kernel, typename... Args>
 cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args... args) {
@@ -1640,7 +1684,36 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int D>
+using PrefixKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefixArgs);
+
+// The prefix kernel for a mode (0-3) and a row-copy index (F = 1, 2, 4); the
+// explicit-mask form (mode 3) has no early variant.
+template <int D, bool EARLY>
+PrefixKernel prefix_kernel_for(int mode, int fi) {
+    if constexpr (EARLY) {
+        const PrefixKernel t[3][3] = {
+            {prefix_pass_kernel<D, 1, 0, true>, prefix_pass_kernel<D, 2, 0, true>,
+             prefix_pass_kernel<D, 4, 0, true>},
+            {prefix_pass_kernel<D, 1, 1, true>, prefix_pass_kernel<D, 2, 1, true>,
+             prefix_pass_kernel<D, 4, 1, true>},
+            {prefix_pass_kernel<D, 1, 2, true>, prefix_pass_kernel<D, 2, 2, true>,
+             prefix_pass_kernel<D, 4, 2, true>}};
+        return t[mode][fi];
+    } else {
+        const PrefixKernel t[4][3] = {
+            {prefix_pass_kernel<D, 1, 0, false>, prefix_pass_kernel<D, 2, 0, false>,
+             prefix_pass_kernel<D, 4, 0, false>},
+            {prefix_pass_kernel<D, 1, 1, false>, prefix_pass_kernel<D, 2, 1, false>,
+             prefix_pass_kernel<D, 4, 1, false>},
+            {prefix_pass_kernel<D, 1, 2, false>, prefix_pass_kernel<D, 2, 2, false>,
+             prefix_pass_kernel<D, 4, 2, false>},
+            {prefix_pass_kernel<D, 1, 3, false>, prefix_pass_kernel<D, 2, 3, false>,
+             prefix_pass_kernel<D, 4, 3, false>}};
+        return t[mode][fi];
+    }
+}
+
+template <int D, bool EARLY>
 cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void* tmap_v,
                             const void* tmap_tk, const void* tmap_tv, cudaStream_t stream) {
     using S = PrefixShape<D>;
@@ -1649,15 +1722,13 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        for (auto k : {prefix_pass_kernel<D, 1, 0>, prefix_pass_kernel<D, 2, 0>,
-                       prefix_pass_kernel<D, 4, 0>, prefix_pass_kernel<D, 1, 1>,
-                       prefix_pass_kernel<D, 2, 1>, prefix_pass_kernel<D, 4, 1>,
-                       prefix_pass_kernel<D, 1, 2>, prefix_pass_kernel<D, 2, 2>,
-                       prefix_pass_kernel<D, 4, 2>, prefix_pass_kernel<D, 1, 3>,
-                       prefix_pass_kernel<D, 2, 3>, prefix_pass_kernel<D, 4, 3>}) {
-            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-        }
+        for (int m = 0; m < (EARLY ? 3 : 4); ++m)
+            for (int fi = 0; fi < 3; ++fi) {
+                const PrefixKernel k = prefix_kernel_for<D, EARLY>(m, fi);
+                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::SMEM_BYTES);
+                if (e != cudaSuccess) return e;
+            }
         configured_for = dev;
     }
     const int G = v.Hq / v.Hkv;
@@ -1696,17 +1767,12 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     const CUtensorMap& ttv = *static_cast<const CUtensorMap*>(tmap_tv);
     const int F = pa.RB == 1 ? replicas_of(M) : 1;
     const int mode = v.dense != nullptr ? kModeDense : v.tmode;
-    using K = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefixArgs);
-    const K table[4][3] = {
-        {prefix_pass_kernel<D, 1, 0>, prefix_pass_kernel<D, 2, 0>, prefix_pass_kernel<D, 4, 0>},
-        {prefix_pass_kernel<D, 1, 1>, prefix_pass_kernel<D, 2, 1>, prefix_pass_kernel<D, 4, 1>},
-        {prefix_pass_kernel<D, 1, 2>, prefix_pass_kernel<D, 2, 2>, prefix_pass_kernel<D, 4, 2>},
-        {prefix_pass_kernel<D, 1, 3>, prefix_pass_kernel<D, 2, 3>, prefix_pass_kernel<D, 4, 3>}};
-    const K kernel = table[mode][F == 4 ? 2 : (F == 2 ? 1 : 0)];
+    const PrefixKernel kernel = prefix_kernel_for<D, EARLY>(mode, F == 4 ? 2 : (F == 2 ? 1 : 0));
     return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, ttk, ttv,
                       pa);
 }
 
+#ifndef TREE_ATTN_EARLY_TU
 template <int D>
 cudaError_t launch_merge_d(const VerifyArgs& v, cudaStream_t stream) {
     const int G = v.Hq / v.Hkv;
@@ -1776,8 +1842,8 @@ __global__ void __launch_bounds__(256)
                       const int32_t* __restrict__ seq_lens, int B, int T, int cols,
                       uint8_t* __restrict__ dense, int32_t* __restrict__ key_lens,
                       int32_t* __restrict__ status) {
+    ptx::grid_dep_wait();    // then let the next kernel start: see tree_mask_kernel
     ptx::grid_dep_launch();
-    ptx::grid_dep_wait();
     const int row = blockIdx.x;  // b * T + t
     const int b = row / T, t = row % T;
     int L = seq_lens[b];
@@ -1812,8 +1878,20 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+#endif  // !TREE_ATTN_EARLY_TU
+
 }  // namespace
 
+#ifdef TREE_ATTN_EARLY_TU
+// The early-start prefix kernels live in their own translation unit
+// (prefix_early.cu includes this file), compiled beside this one.
+cudaError_t launch_prefix_early(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+                                const void* tmap_tk, const void* tmap_tv, cudaStream_t stream) {
+    if (a.d == 128)
+        return launch_prefix_d<128, true>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+    return launch_prefix_d<64, true>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+}
+#else
 cudaError_t launch_dense_mask_build(const uint64_t* mask, int mask_stride,
                                     const int32_t* seq_lens, int B, int T, int dense_cols,
                                     uint8_t* dense, int32_t* key_lens, int32_t* status,
@@ -1832,13 +1910,18 @@ cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64
 
 cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
                           const void* tmap_tk, const void* tmap_tv, cudaStream_t stream) {
-    if (a.d == 128) return launch_prefix_d<128>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
-    return launch_prefix_d<64>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+    if (a.early && a.dense == nullptr)
+        return launch_prefix_early(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+    if (a.d == 128)
+        return launch_prefix_d<128, false>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
+    return launch_prefix_d<64, false>(a, tmap_k, tmap_v, tmap_tk, tmap_tv, stream);
 }
 
 cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream) {
     if (a.d == 128) return launch_merge_d<128>(a, stream);
     return launch_merge_d<64>(a, stream);
 }
+
+#endif  // TREE_ATTN_EARLY_TU
 
 }  // namespace treeattn

@@ -42,6 +42,7 @@ struct VerifyArgs {
     int tmode;
     int ovh;  // overhead slots per unit on the work line (the kernel selector's)
     unsigned long long wait_ns;  // limit of a pipeline wait in the prefix pass
+    int early;  // plan and first committed-prefix loads before the dependency wait
 };
 
 // Enqueue the explicit-mask builder: dense[b][t][p] for p < dense_cols and
@@ -61,6 +62,10 @@ cudaError_t launch_mask_build(const int32_t* parents, int T, int n_trees, uint64
 // All are host memory, copied into the launch.
 cudaError_t launch_prefix(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
                           const void* tmap_tk, const void* tmap_tv, cudaStream_t stream);
+// The same for a.early (in prefix_early.cu): the plan and the first committed
+// prefix loads go out before the dependency wait.
+cudaError_t launch_prefix_early(const VerifyArgs& a, const void* tmap_k, const void* tmap_v,
+                                const void* tmap_tk, const void* tmap_tv, cudaStream_t stream);
 
 // Enqueue the suffix pass + merge (reads the partials in a.ws).
 cudaError_t launch_merge(const VerifyArgs& a, cudaStream_t stream);

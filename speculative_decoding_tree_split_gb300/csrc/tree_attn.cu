@@ -40,6 +40,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Limit of the prefix pass's pipeline waits, read when a call is enqueued.
 std::atomic<unsigned long long> g_wait_ns{TREE_ATTN_DEFAULT_WAIT_NS};
+std::atomic<int> g_early{0};
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -156,10 +157,14 @@ int prefix_impl(VerifyArgs& a, const uint16_t* k_pages, const uint16_t* v_pages,
 
 extern "C" {
 
-int tree_attn_version(void) { return 10100; }
+int tree_attn_version(void) { return 10200; }
 
 unsigned long long tree_attn_set_wait_limit_ns(unsigned long long ns) {
     return g_wait_ns.exchange(ns == 0 ? TREE_ATTN_DEFAULT_WAIT_NS : ns);
+}
+
+int tree_attn_set_early_prefix_loads(int enable) {
+    return g_early.exchange(enable != 0 ? 1 : 0);
 }
 
 int tree_mask_build_batched(const int32_t* parents, int T, int n_trees, uint64_t* mask_out,
@@ -253,6 +258,7 @@ int tree_attn_prefix_pass(const uint16_t* q, const uint16_t* k_pages, const uint
     a.ovh = ovh_for(Hq, Hkv, T);
     a.scale_log2 = to_log2(softmax_scale);
     a.wait_ns = g_wait_ns.load();
+    a.early = g_early.load();
     return prefix_impl(a, k_pages, v_pages, static_cast<cudaStream_t>(stream));
 }
 
@@ -361,6 +367,7 @@ int verify_common(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_
     a.tmode = tmode;
     a.ovh = ovh;
     a.wait_ns = g_wait_ns.load();
+    a.early = g_early.load();
     a.q = q;
     a.k_pages = k_pages;
     a.v_pages = v_pages;

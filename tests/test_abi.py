@@ -38,7 +38,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert ta.version() == 10100
+    assert ta.version() == 10200
 
 
 def test_only_declared_symbols_are_exported(lib):
