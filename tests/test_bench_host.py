@@ -82,7 +82,7 @@ def test_kernel_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     dst = tmp_path / "speculative_decoding_tree_split_gb300" / "csrc"
     dst.mkdir(parents=True)
     texts = {}
-    for name in ("kernels.cu", "layout.h", "ptx.cuh"):
+    for name in ("kernels.cu", "prefix_early.cu", "layout.h", "ptx.cuh"):
         with open(os.path.join(src, name), encoding="utf-8") as f:
             texts[name] = f.read()
 
