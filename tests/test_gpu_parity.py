@@ -343,6 +343,27 @@ def test_merge_rows_per_warp(oracle):
     assert np.array_equal(l2.cpu().numpy(), lse)
 
 
+def test_merge_rows_per_warp_with_many_partials(oracle):
+    # 4 x 16 units of 64 rows, 4096-token prefixes: each unit spans about two
+    # and a half prefix CTAs, so a row has up to four partials (a straddling
+    # CTA leaves its two row copies unfolded); 1024 single-row merge CTAs
+    # would not fit at once, so each merge warp takes two rows in turn.
+    cfg = Config("rpw2", B=4, Hq=128, Hkv=16, d=128, L=4096, page=64, T=8, max_depth=3,
+                 max_branch=3, seed=95)
+    wl = make_workload(cfg)
+    p = ta.plan(4, 128, 16, 128, 8, 64, wl.max_pages_per_seq)
+    assert p["tree_in_prefix"] == 1 and p["merge_rows_per_warp"] == 2
+    assert p["merge_warps_per_row"] == 1
+    x = to_dev(wl)
+    out, lse = ta.verify_tree(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                              x["seq_lens"], x["tree_k"], x["tree_v"], x["parents"],
+                              softmax_scale=wl.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.verify(wl, oracle.tree_mask(wl.parents.tolist()))
+    assert np.abs(out.float().cpu().numpy() - ref_o).max() <= OUT_TOL
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= LSE_TOL
+
+
 @pytest.mark.parametrize("T,G,n_ctas", [(4, 4, 2), (8, 4, 3), (12, 4, 2), (16, 4, 2), (20, 4, 1),
                                         (16, 5, 2)])
 def test_row_replication_paths(oracle, T, G, n_ctas):
