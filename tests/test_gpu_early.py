@@ -81,7 +81,8 @@ SMALL64 = Config("eb", B=2, Hq=10, Hkv=2, d=64, L=(0, 3000), page=16, T=16, max_
 
 
 def _all_layouts(x, wl, n_ctas=0):
-    """(name, out, lse) of every call layout on the same inputs."""
+    """(name, out, lse) of every call layout on the same inputs (the tree in
+    its own buffers; see the paged and explicit-mask variants below)."""
     res = []
     mask = ta.mask_build(x["parents"])
     res.append(("verify",) + ta.verify(x["q"], x["k"], x["v"], x["bt"], x["sl"], x["tk"],
@@ -111,6 +112,34 @@ def test_results_bit_identical_with_and_without(cfg, lens, n_ctas):
     torch.cuda.synchronize()
     for (name, o0, l0), (_, o1, l1) in zip(off, on):
         assert torch.equal(o0, o1) and torch.equal(l0, l1), name
+
+
+@pytest.mark.parametrize("cfg,lens", [(SMALL, [5000, 61, 1290]), (SMALL64, [3000, 17])],
+                         ids=["d128", "d64"])
+def test_tree_in_cache_and_explicit_mask_bit_identical_with_and_without(cfg, lens):
+    # tree tokens padded into the paged cache (their blocks load after the
+    # dependency wait), and the one-pass explicit-mask form (no early start)
+    wl = make_workload(cfg, seq_lens=lens, tree_in_cache=True)
+    x = to_dev(wl)
+    mask = ta.mask_build(x["parents"])
+    cols = ta.dense_cols_for(int(wl.seq_lens.max()) + cfg.T)
+    dense, kl = ta.dense_mask_build(mask, x["sl"], cfg.T, cols)
+
+    def run():
+        a = ta.verify_paged_tree(x["q"], x["k"], x["v"], x["bt"], x["sl"], mask,
+                                 softmax_scale=wl.scale)
+        b = ta.verify_dense(x["q"], x["k"], x["v"], x["bt"], kl, dense, softmax_scale=wl.scale)
+        return a + b
+
+    off = run()
+    prev = ta.set_early_prefix_loads(True)
+    try:
+        on = run()
+    finally:
+        ta.set_early_prefix_loads(prev)
+    torch.cuda.synchronize()
+    for t0, t1 in zip(off, on):
+        assert torch.equal(t0, t1)
 
 
 @pytest.mark.parametrize("name", ["llama8b", "llama70b", "maverick"])
