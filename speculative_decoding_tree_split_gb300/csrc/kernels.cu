@@ -136,6 +136,14 @@ constexpr int kBlock = 2 * kChunk;  // keys per MMA block
 // Block tables of at most this many entries (B * max_pages) are staged in
 // shared memory by the plan, in the same round trip as the sequence lengths.
 constexpr int kSmallBt = 128;
+// Threads of a prefix-pass CTA: the four softmax warps, the copy warp, the
+// MMA warp and a seventh warp that has no role and waits at the final
+// barrier.  Measured on GB300 against the same kernel with six warps: the
+// one-row-copy (Maverick-shaped) pass 92.5 -> 91.0 us, the Llama-3.1-70B
+// pass 57.2 -> 57.0 us, the others unchanged; compiling for 224 threads
+// but launching 192 gave nothing, so the gain comes from the extra warp's
+// presence, by a mechanism these measurements do not identify.
+constexpr int kPrefixThreads = 224;
 // Early start: K/V blocks a CTA loads before its dependency wait.  The plan
 // and the first block's page lookups always go first; each block loaded
 // early also takes memory bandwidth from the tail of the kernel before.
@@ -355,7 +363,7 @@ __device__ __forceinline__ int blocks_of(const Segment& sg) {
 // (q, the tree K/V and the masks are read after it).  The explicit-mask form
 // has no early variant.
 template <int D, int F, int MODE, bool EARLY>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kPrefixThreads, 1)
     prefix_pass_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_tk,
@@ -700,6 +708,8 @@ __global__ void __launch_bounds__(192, 1)
             ptx::mma_commit(bar(S::DRAIN));
             (void)ptx::mbar_wait(bar(S::DRAIN), 0, ptx::kDrainLimitNs);
         }
+    } else if (warp == 6) {
+        // ================= idle (see kPrefixThreads)
     } else {
         // ================= softmax + epilogue warpgroup (warps 0-3)
         constexpr int R = kRows / F;    // tile rows per replica
@@ -1768,8 +1778,8 @@ cudaError_t launch_prefix_d(const VerifyArgs& v, const void* tmap_k, const void*
     const int F = pa.RB == 1 ? replicas_of(M) : 1;
     const int mode = v.dense != nullptr ? kModeDense : v.tmode;
     const PrefixKernel kernel = prefix_kernel_for<D, EARLY>(mode, F == 4 ? 2 : (F == 2 ? 1 : 0));
-    return launch_pdl(kernel, dim3(v.n_ctas), dim3(192), S::SMEM_BYTES, stream, tk, tv, ttk, ttv,
-                      pa);
+    return launch_pdl(kernel, dim3(v.n_ctas), dim3(kPrefixThreads), S::SMEM_BYTES, stream, tk, tv,
+                      ttk, ttv, pa);
 }
 
 #ifndef TREE_ATTN_EARLY_TU
