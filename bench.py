@@ -51,10 +51,10 @@ FALLBACK_HBM_GBS = 6800.0
 # source whose SHA-256 is recorded with it (see profiles/).
 NCU_TRAFFIC = {
     # profiles/prefix_pass_traffic_long_context.md
-    "chain": ("c8e014e5a862b11f", 2376631808),
-    "maverick": ("c8e014e5a862b11f", 541094912),
-    "llama70b": ("c8e014e5a862b11f", 339025920),
-    "llama8b": ("c8e014e5a862b11f", 33741568),
+    "chain": ("3420ca0d31c8ee94", 2376776960),
+    "maverick": ("3420ca0d31c8ee94", 541378048),
+    "llama70b": ("3420ca0d31c8ee94", 339179008),
+    "llama8b": ("3420ca0d31c8ee94", 33742080),
 }
 
 
