@@ -976,14 +976,26 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                         rescale = true;
                     }
                     const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;
+                    // Keys in pairs: one f32x2 fma forms both exponents and one
+                    // f32x2 add folds both probabilities into the running sums
+                    // (key i into sum i & 7, as eight scalar sums would), so
+                    // the issue slots go to the exponentials.
+                    const uint64_t sc2 = ptx::f2_pack(a.scale_log2, a.scale_log2);
+                    const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+                    uint64_t sp2[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) sp2[u] = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < KF; i += 2) {
+                        float x0, x1;
+                        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[i], s[i + 1]), sc2, nm2), x0, x1);
+                        s[i] = ptx::ex2(x0);
+                        s[i + 1] = ptx::ex2(x1);
+                        sp2[(i >> 1) & 3] = ptx::f2_add(sp2[(i >> 1) & 3], ptx::f2_pack(s[i], s[i + 1]));
+                    }
                     float sp[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) sp[u] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < KF; ++i) {
-                        s[i] = ptx::ex2(fmaf(s[i], a.scale_log2, neg_m));
-                        sp[i & 7] += s[i];
-                    }
+                    for (int u = 0; u < 4; ++u) ptx::f2_unpack(sp2[u], sp[2 * u], sp[2 * u + 1]);
                     l_sum += ((sp[0] + sp[1]) + (sp[2] + sp[3])) +
                              ((sp[4] + sp[5]) + (sp[6] + sp[7]));
                 }
