@@ -960,7 +960,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 8; ++u) mp[u] = kNegInf;
 #pragma unroll
-                    for (int i = 0; i < KF; ++i) mp[i & 7] = fmaxf(mp[i & 7], s[i]);
+                    for (int i = 0; i < KF; i += 2)
+                        mp[(i >> 1) & 7] = ptx::fmax3(mp[(i >> 1) & 7], s[i], s[i + 1]);
                     float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
                     mx *= a.scale_log2;
@@ -1009,10 +1010,13 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                     uint32_t pk[KF / 2];
                     // With tracking, sum the rounding errors of the bf16 values
                     // P.V will use, while the pairs are packed (bf16(p) - p).
+                    // A lane without a query row packs whatever its registers
+                    // hold: its P row only reaches its own O row, which is
+                    // never stored.
                     float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int i = 0; i < KF / 2; ++i) {
-                        pk[i] = row_ok ? pack_bf16(s[2 * i], s[2 * i + 1]) : 0u;
+                        pk[i] = pack_bf16(s[2 * i], s[2 * i + 1]);
                         if (track && row_ok) {
                             sr[(2 * i) & 3] += __uint_as_float(pk[i] << 16) - s[2 * i];
                             sr[(2 * i + 1) & 3] +=

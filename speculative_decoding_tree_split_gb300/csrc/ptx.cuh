@@ -247,6 +247,13 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     return r;
 }
 
+// max(a, b, c) in one instruction (three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
