@@ -51,10 +51,10 @@ FALLBACK_HBM_GBS = 6800.0
 # source whose SHA-256 is recorded with it (see profiles/).
 NCU_TRAFFIC = {
     # profiles/prefix_pass_traffic_long_context.md
-    "chain": ("3420ca0d31c8ee94", 2376776960),
-    "maverick": ("3420ca0d31c8ee94", 541378048),
-    "llama70b": ("3420ca0d31c8ee94", 339179008),
-    "llama8b": ("3420ca0d31c8ee94", 33742080),
+    "chain": ("f88e1f9741214b41", 2376858624),
+    "maverick": ("f88e1f9741214b41", 540920576),
+    "llama70b": ("f88e1f9741214b41", 338890496),
+    "llama8b": ("f88e1f9741214b41", 33741824),
 }
 
 
