@@ -1336,10 +1336,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
     suffix_merge_kernel(const MergeArgs a) {
     constexpr int E = D / 32;
     // Accumulator rows each warp loads in the first round trip, together
-    // with the (m, l) of its partials (three with the tree pass, whose
-    // registers are tighter: measured faster there, chain step -0.2 %,
-    // Maverick -0.75 %).
-    constexpr int NF = SUFFIX ? 3 : 4;
+    // with the (m, l) of its partials (the later round trips reuse the same
+    // registers for four rows at a time, so NF is at least 4).
+    constexpr int NF = 4;
+    static_assert(NF >= 4, "the later round trips fill v[0..3]");
     constexpr int R = kRows / F;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
