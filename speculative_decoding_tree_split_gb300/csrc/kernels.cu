@@ -1339,7 +1339,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps, kMergeResident)
     // with the (m, l) of its partials (the later round trips reuse the same
     // registers for four rows at a time, so NF is at least 4).
     constexpr int NF = 4;
-    static_assert(NF >= 4, "the later round trips fill v[0..3]");
     constexpr int R = kRows / F;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
